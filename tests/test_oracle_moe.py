@@ -1,0 +1,212 @@
+"""Pins for the oracle's GEMMs and whole layer (CPU only).
+
+* a per-token brute force with no slot machinery (Python loops, exact
+  rational dot products) must reproduce the grouped oracle;
+* an exact-arithmetic case (all block scales 1, alpha 1) against integer dot
+  products;
+* top-1 with unit weights reduces the layer to a dense per-token FFN;
+* simulated expert parallelism: rank-local outputs sum to the all-expert
+  layer;
+* the tests-page "scale transpose" commit's failure mode (weight scales read
+  as (K_sf, N)) collapses the cosine;
+* SiLU identities.
+"""
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import moe, nvfp4 as q
+from oracle.route import route
+
+F32 = np.float32
+
+
+def _tiny_weights(wl):
+    w1 = np.stack([workloads.expert_w1(wl, e).float().numpy() for e in range(wl.E)])
+    w2 = np.stack([workloads.expert_w2(wl, e).float().numpy() for e in range(wl.E)])
+    return moe.quantize_weights(w1, w2)
+
+
+# independent decoders for the brute force: torch's float8 view for scales and
+# the golden nibble table for codes
+_NIB = {}
+for _line in open(__file__.replace("test_oracle_moe.py", "golden/e2m1_grid.txt")):
+    if _line.strip() and not _line.startswith("#"):
+        a, b = _line.split()
+        _NIB[int(a)] = Fraction(b) if float(b) != 0 else Fraction(0)
+
+
+def _scale(b):
+    return Fraction(float(torch.tensor([int(b)], dtype=torch.uint8).view(torch.float8_e4m3fn).float()))
+
+
+def _row_values(codes_row, sf_row):
+    vals = []
+    for i in range(codes_row.size * 2):
+        byte = int(codes_row[i // 2])
+        nib = (byte >> 4) if i % 2 else (byte & 0xF)
+        vals.append(_NIB[nib] * _scale(sf_row[i // 16]))
+    return vals
+
+
+def _f32(fr):
+    """Nearest fp32 of an exact rational (via fp64; no ties occur here)."""
+    return F32(float(fr))
+
+
+def _bf16(f):
+    return F32(torch.tensor([float(f)], dtype=torch.float32).to(torch.bfloat16).float().item())
+
+
+def _silu_ref(g):
+    e = F32(math.exp(-float(g))) if -float(g) < 88 else F32(np.inf)
+    return F32(F32(g) / (F32(1.0) + e))
+
+
+def test_layer_matches_per_token_brute_force():
+    wl = workloads.small("bf", T=5, K=64, I=64, E=3, topk=2, routing="softmax_topk",
+                         x_kind="outliers")
+    x = workloads.activations(wl).float().numpy()
+    ids, w = workloads.routing(wl)
+    W = _tiny_weights(wl)
+    ref = moe.forward(x, ids, w, wl.E, 0, W)
+
+    xc, xs, gs_x = q.quantize(x)
+    I, K = wl.I, wl.K
+    # L1 + SiLU per (token, j), no slots
+    hs = {}
+    for t in range(wl.T):
+        a = _row_values(xc[t], xs[t])
+        for j in range(wl.topk):
+            e = int(ids[t, j])
+            ag = F32(gs_x * W["gs_w1_gate"][e])
+            au = F32(gs_x * W["gs_w1_up"][e])
+            h = np.empty(I, F32)
+            for n in range(I):
+                wg = _row_values(W["w1_codes"][e, n], W["w1_sf"][e, n])
+                wu = _row_values(W["w1_codes"][e, I + n], W["w1_sf"][e, I + n])
+                g = _bf16(F32(ag * _f32(sum(p * r for p, r in zip(a, wg)))))
+                u = _bf16(F32(au * _f32(sum(p * r for p, r in zip(a, wu)))))
+                h[n] = _bf16(F32(_silu_ref(g) * u))
+            hs[t, j] = h
+    amax = max(float(np.abs(v).max()) for v in hs.values())
+    gs_h = F32(F32(amax) / F32(2688.0))
+    out = np.zeros((wl.T, K), F32)
+    for t in range(wl.T):
+        acc = np.zeros(K, F32)
+        for j in range(wl.topk):
+            e = int(ids[t, j])
+            hc, hsf, _ = q.quantize(hs[t, j][None, :], gs_h)
+            hv = _row_values(hc[0], hsf[0])
+            a2 = F32(gs_h * W["gs_w2"][e])
+            y = np.array([_bf16(F32(a2 * _f32(sum(p * r for p, r in zip(
+                hv, _row_values(W["w2_codes"][e, n], W["w2_sf"][e, n])))))) for n in range(K)], F32)
+            acc = acc + F32(w[t, j]) * y
+        out[t] = q.bf16_round(acc)
+    assert ref["gs_h"] == gs_h
+    assert np.array_equal(ref["out"], out)
+
+
+def test_exact_arithmetic_gemm_equals_integer_dot_products():
+    r = np.random.default_rng(11)
+    M, N, K = 7, 9, 128
+    ac = r.integers(0, 256, (M, K // 2)).astype(np.uint8)
+    wc = r.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    ones_a = np.full((M, K // 16), 0x38, np.uint8)
+    ones_w = np.full((N, K // 16), 0x38, np.uint8)
+    acc = moe.expert_gemm(ac, ones_a, wc, ones_w)
+    # integer arithmetic in units of 1/4: value*2 is an integer for every code
+    def ints(c):
+        nib = np.stack([c & 0xF, c >> 4], -1).reshape(c.shape[0], -1)
+        mag = np.array([0, 1, 2, 3, 4, 6, 8, 12])[nib & 7]
+        return np.where(nib & 8, -mag, mag).astype(np.int64)
+    exact = ints(ac) @ ints(wc).T            # = 4 * sum
+    assert np.array_equal(acc * 4, exact.astype(np.float32))
+
+
+def test_gemm_is_the_exact_sum_rounded_once():
+    """Closed form: with random scales the fp64 contraction, rounded to fp32,
+    equals the exact rational sum rounded to fp32 (within one fp32 ulp for the
+    double rounding)."""
+    r = np.random.default_rng(12)
+    M, N, K = 3, 4, 96
+    ac = r.integers(0, 256, (M, K // 2)).astype(np.uint8)
+    wc = r.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    asf = r.integers(0x10, 0x60, (M, K // 16)).astype(np.uint8)
+    wsf = r.integers(0x10, 0x60, (N, K // 16)).astype(np.uint8)
+    acc = moe.expert_gemm(ac, asf, wc, wsf)
+    for m in range(M):
+        a = _row_values(ac[m], asf[m])
+        for n in range(N):
+            ex = sum(p * q_ for p, q_ in zip(a, _row_values(wc[n], wsf[n])))
+            ref = F32(float(ex))
+            assert abs(acc[m, n] - ref) <= np.spacing(np.abs(ref))
+
+
+def test_top1_unit_weight_is_a_dense_ffn():
+    wl = workloads.small("d", T=6, K=64, I=64, E=4, topk=1)
+    x = workloads.activations(wl).float().numpy()
+    ids = np.array([[0], [3], [1], [0], [2], [3]], np.int32)
+    w = np.ones((6, 1), np.float32)
+    W = _tiny_weights(wl)
+    res = moe.forward(x, ids, w, 4, 0, W)
+    ps = res["route"]["pair_slot"]
+    assert np.array_equal(res["out"], res["y"][ps])
+
+
+def test_simulated_expert_parallel_ranks_sum_to_all_experts():
+    """The "global expert ids" commit: each rank computes its local experts'
+    share; the caller's reduction of the rank outputs gives the full layer."""
+    wl = workloads.small("ep", T=12, K=64, I=64, E=16, topk=3)
+    x = workloads.activations(wl).float().numpy()
+    ids, w = workloads.routing(wl)
+    W = _tiny_weights(wl)
+    gs_h = F32(1.0 / 2688.0)
+    full = moe.forward(x, ids, w, 16, 0, W, gs_h=gs_h)["out"]
+    total = np.zeros_like(full)
+    for rank in range(4):
+        sl = slice(4 * rank, 4 * rank + 4)
+        Wr = {k: (v[sl] if isinstance(v, np.ndarray) and v.shape[0] == 16 else v)
+              for k, v in W.items()}
+        total += moe.forward(x, ids, w, 4, 4 * rank, Wr, gs_h=gs_h)["out"]
+    err = np.abs(total - full).max()
+    assert err <= 1e-2 * np.abs(full).max()
+    cos = (total * full).sum() / np.sqrt((total ** 2).sum() * (full ** 2).sum())
+    assert cos > 0.9999
+
+
+def test_transposed_weight_scales_collapse_the_output():
+    """Mirror of the tests-page "scale transpose" commit: scales stored as
+    (N, K_sf) but read as if they were (K_sf, N) scramble the layer."""
+    wl = workloads.small("m2", T=32, K=128, I=128, E=2, topk=1)
+    x = workloads.activations(wl).float().numpy()
+    ids, w = workloads.routing(wl)
+    W = _tiny_weights(wl)
+    good = moe.forward(x, ids, w, 2, 0, W)["out"]
+    bad_w = dict(W)
+    E, N, ksf = W["w1_sf"].shape
+    bad_w["w1_sf"] = W["w1_sf"].transpose(0, 2, 1).reshape(E, N, ksf).copy()
+    bad = moe.forward(x, ids, w, 2, 0, bad_w)["out"]
+    cos = (good * bad).sum() / np.sqrt((good ** 2).sum() * (bad ** 2).sum())
+    assert cos < 0.95
+
+
+def test_silu_identities():
+    g = q.bf16_round(np.random.default_rng(13).standard_normal(10000).astype(F32) * 8)
+    one = np.ones_like(g)
+    s = moe.silu_mul(g, one)           # bf16(silu(g))
+    assert moe.silu_mul(np.zeros(1, F32), np.ones(1, F32))[0] == 0.0
+    # silu(x) - silu(-x) = x  (each side rounded to bf16: within 2 bf16 ulps of x)
+    d = s - moe.silu_mul(-g, one)
+    assert np.all(np.abs(d - g) <= 2 * np.abs(g) * 2.0 ** -8 + 1e-30)
+    # against an fp64 reference
+    ref = g.astype(np.float64) / (1 + np.exp(-g.astype(np.float64)))
+    assert np.all(np.abs(s - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+    # large negative gate -> -0/0, large positive -> g
+    assert moe.silu_mul(np.array([-200.0], F32), np.ones(1, F32))[0] == 0.0
+    assert moe.silu_mul(np.array([200.0], F32), np.ones(1, F32))[0] == 200.0
