@@ -1,0 +1,267 @@
+/*
+ * moe_stage.h -- C ABI of the NVFP4 routed-expert MoE stage for GB300 (sm_103a).
+ *
+ * The layer this library computes is the one described on the nvfp4-megamoe-kernel
+ * commit pages (commits of src/nvfp4_megamoe_kernel/nvfp4_mega_moe.py, of src, of
+ * vllm/nvfp4_cutedsl.py and of tests):
+ *
+ *   x (BF16) --global scale amax/2688--> NVFP4 (E2M1 codes + UE4M3 block scales, 16/block)
+ *     --route (token,k) pairs to experts--> slot rows grouped by expert
+ *     --L1 grouped GEMM [gate|up], alpha = gs_x * gs_w--> BF16 g, u
+ *     --SiLU(g) * u--> BF16 h --requantise--> NVFP4
+ *     --L2 grouped GEMM (down), alpha = gs_h * gs_w2--> BF16 y
+ *     --scatter-add weighted by the routing weights--> rank-local output (BF16).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Memory: every pointer argument is DEVICE memory owned by the caller, unless
+ *    the argument says otherwise.  The library never allocates, frees or caches
+ *    device memory; scratch space is the caller's `ws` buffer, sized by the
+ *    *_workspace_size queries.  All buffers must be 256-byte aligned except where
+ *    noted (BF16 tensors: 16 bytes).
+ *  - Work is enqueued on the caller's stream, never synchronises the host, and
+ *    can be captured into a CUDA graph (no host reads of device data).
+ *  - Return value: MOE_OK, or an error found on the host before anything was
+ *    enqueued (MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE),
+ *    or MOE_ERR_CUDA if a launch failed.
+ *  - Device-side errors (a bounded wait that gave up, an index that failed its
+ *    bounds check) are written to the optional `dev_status` word (int32, device
+ *    memory; first error wins, never cleared by the library) and the kernel
+ *    returns early.  Read it after synchronising.
+ *  - Byte formats: NVFP4 codes are sign-magnitude E2M1 nibbles, two per byte,
+ *    the even-K element in the low nibble.  Block scales are UE4M3 (float8 e4m3fn,
+ *    sign 0) bytes, one per 16 consecutive elements along the contraction axis.
+ *    "Swizzled" scales use the block-scaled MMA layout: 512-byte atoms of 128 rows
+ *    x 4 scale columns, offset in atom = 16*(m%32) + 4*((m/32)%4) + (k%4), atom
+ *    index = (m/128)*(K/64) + k/4.
+ */
+#ifndef MOE_STAGE_H
+#define MOE_STAGE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* moe_stream_t;
+
+typedef int moe_status;
+#define MOE_OK                    0
+#define MOE_ERR_INVALID_ARG       1  /* null pointer, bad enum, misalignment, negative size */
+#define MOE_ERR_UNSUPPORTED_SHAPE 2  /* K % 128, I % 64, E > 256, topk > 32, ... */
+#define MOE_ERR_WORKSPACE         3  /* ws_bytes smaller than the size query's answer */
+#define MOE_ERR_CUDA              4  /* a CUDA launch or tensor-map encode failed */
+#define MOE_ERR_TIMEOUT           5  /* device: a bounded wait gave up (dev_status only) */
+#define MOE_ERR_DEVICE_INDEX      6  /* device: an index failed its bounds check (dev_status only) */
+
+/* Text for a status code (static storage). */
+const char* moe_status_string(moe_status s);
+
+/* Rows of one MMA tile: each expert's slot range is padded to a multiple of it. */
+#define MOE_TILE_M 128
+
+/* Scale layouts for moe_stage_activation. */
+#define MOE_SF_ROWMAJOR 0  /* [rows, K/16] bytes */
+#define MOE_SF_SWIZZLED 1  /* MMA layout, rows padded to 128 */
+
+/* Weight kinds for moe_prepare_weights. */
+#define MOE_PREP_W1 0      /* gate|up projection, [E, 2I, K]  */
+#define MOE_PREP_W2 1      /* down projection,    [E, K, I]   */
+
+/* L1 epilogues. */
+#define MOE_L1_GATEUP_BF16   0  /* store g | u as BF16 [slots, 2I] */
+#define MOE_L1_SILU_BF16     1  /* store h = bf16(silu(g)*u) [slots, I] and max|h| */
+#define MOE_L1_SILU_REQUANT  2  /* quantise h with a fixed global scale to NVFP4 */
+
+/* L2 epilogues. */
+#define MOE_L2_ROWS_BF16 0      /* store y as BF16 [slots, K] */
+#define MOE_L2_SCATTER   1      /* out32[token] += weight * y (fp32 atomics) */
+
+/* Global-scale modes for the requantised activation h in moe_forward. */
+#define MOE_GS_DYNAMIC 0        /* gs_h = max|h| / 2688 over this call's slots */
+#define MOE_GS_FIXED   1        /* gs_h supplied by the caller (calibrated) */
+
+/* ------------------------------------------------------------------------- */
+/* Size queries (host only, no device work).                                  */
+/* ------------------------------------------------------------------------- */
+
+/* Slot capacity for T tokens, top-k and E local experts: an upper bound on the
+ * padded slot count, T*topk + 127*E rounded up to a multiple of 128.  Every
+ * slot-indexed buffer (slot_token, slot_weight, activation/h codes and scales)
+ * holds this many rows.  Returns -1 on bad arguments. */
+int64_t moe_slot_capacity(int64_t T, int topk, int E);
+
+/* Scratch bytes moe_route needs. */
+size_t moe_route_workspace_size(int64_t T, int topk, int E);
+
+/* Scratch bytes moe_stage_activation / moe_stage_activation_to_slots need. */
+size_t moe_stage_workspace_size(void);
+
+/* Scratch bytes moe_forward needs for up to T_max tokens. */
+size_t moe_workspace_size(int64_t T_max, int K, int I, int E, int topk);
+
+/* ------------------------------------------------------------------------- */
+/* Setup (not on the per-call path)                                          */
+/* ------------------------------------------------------------------------- */
+
+/* Rearrange weight block scales into the layout the grouped GEMMs read.
+ * Source: the tests-page "scale transpose" commit -- checkpoint weight scales
+ * are (N, K_sf) row-major per expert.
+ *   sf_rowmajor: [E, N, K/16] UE4M3 bytes (N = 2I for MOE_PREP_W1, rows 0..I-1
+ *                gate and I..2I-1 up; N = K_out for MOE_PREP_W2).
+ *   sf_prepared: E*N*K/16 bytes, written.  For MOE_PREP_W2 it is the swizzled
+ *                layout of each expert's [N, K/16] matrix.  For MOE_PREP_W1 the
+ *                rows are first regrouped so that every 128-row atom holds 64
+ *                gate rows followed by the 64 matching up rows (the L1 tile
+ *                computes 64 h columns from both halves).
+ *   N % 128 == 0, K % 64 == 0.  Buffers may be any alignment. */
+moe_status moe_prepare_weights(const uint8_t* sf_rowmajor, uint8_t* sf_prepared,
+                               int E, int N, int K, int kind, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Per-call path                                                              */
+/* ------------------------------------------------------------------------- */
+
+/* Quantise a BF16 tensor to NVFP4 (stage_activation of the nvfp4_mega_moe.py
+ * commits: returns codes, scales and the global scale).
+ *   x:        [T, K] BF16, row stride ld_x elements (ld_x >= K, ld_x % 8 == 0).
+ *   x_fp4:    [T, K/2] codes, written.
+ *   x_sf:     MOE_SF_ROWMAJOR: [T, K/16]; MOE_SF_SWIZZLED: ceil(T/128)*128*K/16.
+ *   gs_out:   one fp32, written with the global scale used.
+ *   gs_fixed: NULL -> gs = max|x| / 2688 (two passes over x); else one fp32
+ *             holding a fixed global scale (one pass; the calibrated mode of the
+ *             vllm/nvfp4_cutedsl.py commits).
+ *   Arithmetic (fp32, round-to-nearest-even): rg = 1/gs (saturated to FLT_MAX);
+ *   per 16-block s = (max|x|*rg)/6 -> UE4M3 (RNE, saturating at 448); each
+ *   element (|x|*rg) * (1/decode(s)) -> nearest E2M1 (ties to even, saturating
+ *   at 6); bit 3 = sign bit of x; a zero scale gives sign-only nibbles.
+ *   K % 64 == 0.  ws: moe_stage_workspace_size() bytes. */
+moe_status moe_stage_activation(const void* x, int64_t T, int K, int64_t ld_x,
+                                uint8_t* x_fp4, uint8_t* x_sf, int sf_layout,
+                                float* gs_out, const float* gs_fixed,
+                                void* ws, size_t ws_bytes, int32_t* dev_status,
+                                moe_stream_t stream);
+
+/* The same quantisation, written straight into the slot rows the router chose
+ * (the activation gather of the src commits fused into the quantiser):
+ * token t's codes go to every slot pair_slot[t*topk + j] >= 0.
+ *   a_fp4: [capacity, K/2]; a_sf: capacity*K/16 bytes, swizzled.
+ *   Padding slot rows are not written (the GEMMs never read them into valid
+ *   outputs). */
+moe_status moe_stage_activation_to_slots(const void* x, int64_t T, int K, int64_t ld_x,
+                                         const int32_t* pair_slot, int topk, int64_t capacity,
+                                         uint8_t* a_fp4, uint8_t* a_sf,
+                                         float* gs_out, const float* gs_fixed,
+                                         void* ws, size_t ws_bytes, int32_t* dev_status,
+                                         moe_stream_t stream);
+
+/* Route (token, k) pairs to expert-grouped slots (the slot routing of the src and
+ * vllm/nvfp4_cutedsl.py commits: local ids, bincount + cumsum offsets in int32,
+ * stable grouping by expert, zero-weight padding).
+ *   topk_ids [T, topk] int32 GLOBAL expert ids; local = id - expert_offset; pairs
+ *   with local outside [0, E) are dropped.  topk_w [T, topk] fp32.
+ *   Outputs (all written): counts [E], offsets [E+1] (exclusive cumsum of counts),
+ *   padded_offsets [E+1] (cumsum of counts rounded up to 128), slot_token
+ *   [capacity] (token of each slot, -1 for padding), slot_weight [capacity] (0 for
+ *   padding), pair_slot [T*topk] (slot of each pair, -1 if dropped).  Within an
+ *   expert, slots follow ascending t*topk + j.
+ *   capacity >= moe_slot_capacity(T, topk, E).  E <= 256, topk <= 32.
+ *   ws: moe_route_workspace_size(T, topk, E) bytes. */
+moe_status moe_route(const int32_t* topk_ids, const float* topk_w, int64_t T, int topk,
+                     int E, int expert_offset,
+                     int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                     int32_t* slot_token, float* slot_weight, int32_t* pair_slot,
+                     int64_t capacity, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* L1 grouped GEMM, gate|up (nvfp4_mega_moe_l1 of the nvfp4_mega_moe.py commits;
+ * split at I per the vllm/nvfp4_cutedsl.py "intermediate_size" commit).
+ * For every expert e and slot row p in [padded_offsets[e], padded_offsets[e] +
+ * offsets[e+1] - offsets[e]):
+ *   acc[p, n] = sum_k deq(A)[p, k] * deq(W1[e])[n, k]     (fp32 accumulate)
+ *   g = bf16(gs_a * gs_w1_gate[e] * acc[:, 0:I]),  u = bf16(gs_a * gs_w1_up[e] * acc[:, I:2I])
+ *   a_fp4 [capacity, K/2], a_sf swizzled (capacity*K/16); gs_a one fp32.
+ *   w1_fp4 [E, 2I, K/2]; w1_sf prepared by moe_prepare_weights(MOE_PREP_W1).
+ *   epilogue:
+ *     MOE_L1_GATEUP_BF16: out_bf16 [capacity, 2I] gets g | u.
+ *     MOE_L1_SILU_BF16:   out_bf16 [capacity, I] gets h = bf16(silu(g)*u),
+ *                         silu(g) = g/(1+exp(-g)) in fp32; if h_amax != NULL it is
+ *                         set to max|h| over valid rows (fp32, zeroed by this call).
+ *     MOE_L1_SILU_REQUANT: h is quantised with the fixed global scale *gs_h (as in
+ *                         moe_stage_activation) into h_fp4 [capacity, I/2] and
+ *                         h_sf (swizzled, capacity*I/16); out_bf16 may be NULL or
+ *                         receive h as well.
+ *   Rows of padding are never written.  K % 128 == 0, I % 64 == 0, E <= 256. */
+moe_status moe_grouped_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a,
+                               const int32_t* offsets, const int32_t* padded_offsets,
+                               int E, int64_t capacity, int K, int I,
+                               const uint8_t* w1_fp4, const uint8_t* w1_sf,
+                               const float* gs_w1_gate, const float* gs_w1_up,
+                               int epilogue, void* out_bf16, float* h_amax,
+                               uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h,
+                               int32_t* dev_status, moe_stream_t stream);
+
+/* Requantise h [capacity, I] BF16 rows to NVFP4 with gs_h = h_amax[0]/2688
+ * (written to gs_h_out), skipping padding rows (slot_token < 0): the
+ * stage_activation of h of the nvfp4_mega_moe.py "global scale" commit.
+ * h_fp4 [capacity, I/2]; h_sf swizzled.  I % 64 == 0. */
+moe_status moe_requant(const void* h, int64_t capacity, int I, const int32_t* slot_token,
+                       const float* h_amax, float* gs_h_out, uint8_t* h_fp4, uint8_t* h_sf,
+                       int32_t* dev_status, moe_stream_t stream);
+
+/* L2 grouped GEMM, down projection (nvfp4_mega_moe_l2), same slot order as L1:
+ *   y[p, n] = bf16(gs_h * gs_w2[e] * sum_i deq(H)[p, i] * deq(W2[e])[n, i])
+ *   h_fp4 [capacity, I/2], h_sf swizzled; w2_fp4 [E, K, I/2]; w2_sf prepared
+ *   (MOE_PREP_W2).
+ *   epilogue MOE_L2_ROWS_BF16: y_rows [capacity, K] BF16.
+ *   epilogue MOE_L2_SCATTER: out32[slot_token[p], :] += slot_weight[p] * y[p, :]
+ *   (fp32 atomic adds; out32 [T, K] is NOT cleared by this call).
+ *   K % 128 == 0, I % 64 == 0. */
+moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h,
+                               const int32_t* offsets, const int32_t* padded_offsets,
+                               int E, int64_t capacity, int I, int K,
+                               const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2,
+                               int epilogue, void* y_rows,
+                               const int32_t* slot_token, const float* slot_weight,
+                               float* out32, int64_t T,
+                               int32_t* dev_status, moe_stream_t stream);
+
+/* out_bf16[i] = bf16(out32[i]) for i < T*K (round to nearest even). */
+moe_status moe_cast_output(const float* out32, void* out_bf16, int64_t T, int K,
+                           moe_stream_t stream);
+
+/* Expert weights of one rank, all device memory. */
+typedef struct moe_weights {
+    const uint8_t* w1_fp4;      /* [E, 2I, K/2]                          */
+    const uint8_t* w1_sf;       /* prepared, MOE_PREP_W1                 */
+    const float*   gs_w1_gate;  /* [E]                                   */
+    const float*   gs_w1_up;    /* [E]                                   */
+    const uint8_t* w2_fp4;      /* [E, K, I/2]                           */
+    const uint8_t* w2_sf;       /* prepared, MOE_PREP_W2                 */
+    const float*   gs_w2;       /* [E]                                   */
+} moe_weights;
+
+/* The whole rank-local layer (nvfp4_moe_full / the CuTeDSL runner's forward):
+ * route -> quantise x into slots -> L1 (+SiLU*up, +requant) -> L2 (+weighted
+ * scatter) -> BF16 output.  The caller sums outputs across ranks.
+ *   x [T, K] BF16 (row stride K); topk_ids/topk_w [T, topk]; out [T, K] BF16.
+ *   gs_x_fixed: NULL -> amax of x; else a fixed fp32 global scale.
+ *   gs_h_mode MOE_GS_DYNAMIC: gs_h (device fp32) receives max|h|/2688;
+ *   MOE_GS_FIXED: gs_h holds the scale to use (h quantised in the L1 epilogue).
+ *   ws: moe_workspace_size(T, K, I, E, topk) bytes (T <= the T_max it was sized for).
+ *   Tokens none of whose experts are local get 0. */
+moe_status moe_forward(const void* x, int64_t T, int K, int I, int E,
+                       const int32_t* topk_ids, const float* topk_w, int topk,
+                       int expert_offset, const moe_weights* w,
+                       const float* gs_x_fixed, int gs_h_mode, float* gs_h,
+                       void* out, int32_t* dev_status,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_STAGE_H */

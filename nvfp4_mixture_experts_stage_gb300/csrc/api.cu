@@ -1,0 +1,351 @@
+// C ABI of the NVFP4 MoE stage: argument checks, workspace carving and launches.
+// Every entry point only enqueues work on the caller's stream.
+#include <cstdio>
+
+#include <algorithm>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+int64_t route_chunks(int64_t T, int topk) { return ceil_div(T * topk, kRouteChunk); }
+
+// Bump allocator over the caller's workspace.
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count) {
+    T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off += align256(count * sizeof(T));
+    return p;
+  }
+};
+
+moe_status quantize_launch(int dst, const void* x, int64_t rows, int K, int64_t ld_x, const uint32_t* amax_bits,
+                           const float* gs_fixed, float* gs_out, uint8_t* codes, uint8_t* sf,
+                           const int32_t* pair_slot, int topk, const int32_t* slot_token, int64_t capacity,
+                           int32_t* status, cudaStream_t st) {
+  QuantArgs a;
+  a.x = reinterpret_cast<const uint4*>(x);
+  a.rows = rows;
+  a.K = K;
+  a.ld_vec = ld_x / 8;
+  a.amax_bits = amax_bits;
+  a.gs_fixed = gs_fixed;
+  a.gs_out = gs_out;
+  a.codes = codes;
+  a.sf = sf;
+  a.pair_slot = pair_slot;
+  a.topk = topk;
+  a.slot_token = slot_token;
+  a.capacity = capacity;
+  a.status = status;
+  const int64_t warps = rows * ceil_div(K, 256);
+  if (warps >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int blocks = (int)std::min<int64_t>(std::max<int64_t>(ceil_div(warps, 8 * 4), 1), (int64_t)sm_count() * 8);
+  return launch_quantize(dst, a, blocks, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status amax_launch(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, cudaStream_t st) {
+  if (cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  const int64_t vecs = rows * (K / 8);
+  if (vecs == 0) return MOE_OK;
+  if (vecs >= (int64_t(1) << 32)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int blocks = (int)std::min<int64_t>(std::max<int64_t>(ceil_div(vecs, 256 * 4), 1), (int64_t)sm_count() * 8);
+  return launch_amax(x, rows, K, ld_x, amax_bits, blocks, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status route_impl(const int32_t* ids, const float* w, int64_t T, int topk, int E, int off, int32_t* counts,
+                      int32_t* offsets, int32_t* poff, int32_t* slot_token, float* slot_weight, int32_t* pair_slot,
+                      int64_t capacity, int32_t* cnt, int32_t* base, int32_t* status, cudaStream_t st) {
+  if (cudaMemsetAsync(slot_token, 0xFF, capacity * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(slot_weight, 0, capacity * sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
+  const int nchunks = (int)route_chunks(T, topk);
+  return launch_route(ids, w, T * topk, topk, E, off, cnt, base, nchunks, counts, offsets, poff, slot_token,
+                      slot_weight, pair_slot, capacity, status, st) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+bool shape_ok(int K, int I, int E) {
+  return K > 0 && I > 0 && K % 128 == 0 && I % 64 == 0 && E >= 1 && E <= 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, bad enum, misalignment or negative size)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (needs K % 128 == 0, I % 64 == 0, 1 <= E <= 256, 1 <= topk <= 32)";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA launch or tensor-map encode failed";
+    case MOE_ERR_TIMEOUT: return "device: a bounded wait gave up";
+    case MOE_ERR_DEVICE_INDEX: return "device: an index failed its bounds check";
+  }
+  return "unknown status";
+}
+
+int64_t moe_slot_capacity(int64_t T, int topk, int E) {
+  if (T < 0 || topk < 1 || E < 1) return -1;
+  return ceil_div(T * topk + (int64_t)(kTileM - 1) * E, kTileM) * kTileM;
+}
+
+size_t moe_route_workspace_size(int64_t T, int topk, int E) {
+  if (T < 0 || topk < 1 || E < 1) return 0;
+  const int64_t n = route_chunks(T, topk) * E;
+  return 2 * align256(std::max<int64_t>(n, 1) * sizeof(int32_t));
+}
+
+size_t moe_stage_workspace_size(void) { return 256; }
+
+static size_t forward_layout(Carve& c, int64_t T, int K, int I, int E, int topk, void** parts) {
+  const int64_t cap = moe_slot_capacity(T, topk, E);
+  parts[0] = c.take<uint32_t>(64);                                   // scalars
+  parts[1] = c.take<uint8_t>(moe_route_workspace_size(T, topk, E));  // route tables
+  parts[2] = c.take<int32_t>(E);                                     // counts
+  parts[3] = c.take<int32_t>(E + 1);                                 // offsets
+  parts[4] = c.take<int32_t>(E + 1);                                 // padded offsets
+  parts[5] = c.take<int32_t>(cap);                                   // slot_token
+  parts[6] = c.take<float>(cap);                                     // slot_weight
+  parts[7] = c.take<int32_t>(std::max<int64_t>(T * topk, 1));        // pair_slot
+  parts[8] = c.take<uint8_t>(cap * K / 2);                           // A codes
+  parts[9] = c.take<uint8_t>(cap * K / 16);                          // A scales
+  parts[10] = c.take<uint16_t>(cap * I);                             // h bf16
+  parts[11] = c.take<uint8_t>(cap * I / 2);                          // h codes
+  parts[12] = c.take<uint8_t>(cap * I / 16);                         // h scales
+  parts[13] = c.take<float>(std::max<int64_t>(T * K, 1));            // out32
+  return c.off;
+}
+
+size_t moe_workspace_size(int64_t T_max, int K, int I, int E, int topk) {
+  if (T_max < 0 || !shape_ok(K, I, E) || topk < 1 || topk > 32) return 0;
+  Carve c{nullptr};
+  void* parts[14];
+  return forward_layout(c, T_max, K, I, E, topk, parts);
+}
+
+moe_status moe_prepare_weights(const uint8_t* sf_rowmajor, uint8_t* sf_prepared, int E, int N, int K, int kind,
+                               moe_stream_t stream) {
+  if (!sf_rowmajor || !sf_prepared || E < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (kind != MOE_PREP_W1 && kind != MOE_PREP_W2) return MOE_ERR_INVALID_ARG;
+  if (N % 128 || K % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int64_t total = (int64_t)E * N * (K / 16);
+  const int blocks = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)sm_count() * 16);
+  return launch_prepare_weight_sf(sf_rowmajor, sf_prepared, E, N, K / 16, kind == MOE_PREP_W1, blocks, stream) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+moe_status moe_stage_activation(const void* x, int64_t T, int K, int64_t ld_x, uint8_t* x_fp4, uint8_t* x_sf,
+                                int sf_layout, float* gs_out, const float* gs_fixed, void* ws, size_t ws_bytes,
+                                int32_t* dev_status, moe_stream_t stream) {
+  if (T < 0 || K <= 0 || ld_x < K) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !x_fp4 || !x_sf)) return MOE_ERR_INVALID_ARG;
+  if (!gs_out || (!gs_fixed && !ws)) return MOE_ERR_INVALID_ARG;
+  if (sf_layout != MOE_SF_ROWMAJOR && sf_layout != MOE_SF_SWIZZLED) return MOE_ERR_INVALID_ARG;
+  if (K % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ld_x % 8 || !aligned(x, 16) || !aligned(x_fp4, 4) || !aligned(x_sf, 4)) return MOE_ERR_INVALID_ARG;
+  if (!gs_fixed && ws_bytes < moe_stage_workspace_size()) return MOE_ERR_WORKSPACE;
+  uint32_t* amax = reinterpret_cast<uint32_t*>(ws);
+  if (!gs_fixed) {
+    moe_status s = amax_launch(x, T, K, ld_x, amax, stream);
+    if (s != MOE_OK) return s;
+  }
+  return quantize_launch(sf_layout == MOE_SF_ROWMAJOR ? 0 : 1, x, T, K, ld_x, gs_fixed ? nullptr : amax, gs_fixed,
+                         gs_out, x_fp4, x_sf, nullptr, 0, nullptr, 0, dev_status, stream);
+}
+
+moe_status moe_stage_activation_to_slots(const void* x, int64_t T, int K, int64_t ld_x, const int32_t* pair_slot,
+                                         int topk, int64_t capacity, uint8_t* a_fp4, uint8_t* a_sf, float* gs_out,
+                                         const float* gs_fixed, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                         moe_stream_t stream) {
+  if (T < 0 || K <= 0 || ld_x < K || topk < 1 || topk > 32 || capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !pair_slot || !a_fp4 || !a_sf)) return MOE_ERR_INVALID_ARG;
+  if (!gs_out || (!gs_fixed && !ws)) return MOE_ERR_INVALID_ARG;
+  if (K % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (capacity % kTileM) return MOE_ERR_INVALID_ARG;
+  if (ld_x % 8 || !aligned(x, 16) || !aligned(a_fp4, 4) || !aligned(a_sf, 4)) return MOE_ERR_INVALID_ARG;
+  if (!gs_fixed && ws_bytes < moe_stage_workspace_size()) return MOE_ERR_WORKSPACE;
+  uint32_t* amax = reinterpret_cast<uint32_t*>(ws);
+  if (!gs_fixed) {
+    moe_status s = amax_launch(x, T, K, ld_x, amax, stream);
+    if (s != MOE_OK) return s;
+  }
+  return quantize_launch(2, x, T, K, ld_x, gs_fixed ? nullptr : amax, gs_fixed, gs_out, a_fp4, a_sf, pair_slot,
+                         topk, nullptr, capacity, dev_status, stream);
+}
+
+moe_status moe_route(const int32_t* topk_ids, const float* topk_w, int64_t T, int topk, int E, int expert_offset,
+                     int32_t* counts, int32_t* offsets, int32_t* padded_offsets, int32_t* slot_token,
+                     float* slot_weight, int32_t* pair_slot, int64_t capacity, void* ws, size_t ws_bytes,
+                     moe_stream_t stream) {
+  if (T < 0 || topk < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 256 || topk > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!counts || !offsets || !padded_offsets || !slot_token || !slot_weight || !ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !topk_w || !pair_slot)) return MOE_ERR_INVALID_ARG;
+  if (capacity < moe_slot_capacity(T, topk, E)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_route_workspace_size(T, topk, E)) return MOE_ERR_WORKSPACE;
+  const size_t half = moe_route_workspace_size(T, topk, E) / 2;
+  int32_t* cnt = reinterpret_cast<int32_t*>(ws);
+  int32_t* base = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ws) + half);
+  return route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, padded_offsets, slot_token,
+                    slot_weight, pair_slot, capacity, cnt, base, nullptr, stream);
+}
+
+moe_status moe_grouped_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,
+                               const int32_t* padded_offsets, int E, int64_t capacity, int K, int I,
+                               const uint8_t* w1_fp4, const uint8_t* w1_sf, const float* gs_w1_gate,
+                               const float* gs_w1_up, int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4,
+                               uint8_t* h_sf, const float* gs_h, int32_t* dev_status, moe_stream_t stream) {
+  if (!a_fp4 || !a_sf || !gs_a || !offsets || !padded_offsets || !w1_fp4 || !w1_sf || !gs_w1_gate || !gs_w1_up)
+    return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(K, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (capacity <= 0 || capacity % kTileM || capacity > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a_fp4, 16) || !aligned(w1_fp4, 16) || !aligned(a_sf, 16) || !aligned(w1_sf, 16))
+    return MOE_ERR_INVALID_ARG;
+  switch (epilogue) {
+    case MOE_L1_GATEUP_BF16:
+    case MOE_L1_SILU_BF16:
+      if (!out_bf16 || !aligned(out_bf16, 16)) return MOE_ERR_INVALID_ARG;
+      break;
+    case MOE_L1_SILU_REQUANT:
+      if (!h_fp4 || !h_sf || !gs_h || !aligned(h_fp4, 8) || !aligned(h_sf, 4)) return MOE_ERR_INVALID_ARG;
+      if (out_bf16 && !aligned(out_bf16, 16)) return MOE_ERR_INVALID_ARG;
+      break;
+    default: return MOE_ERR_INVALID_ARG;
+  }
+  return launch_gemm_l1(a_fp4, a_sf, gs_a, offsets, padded_offsets, E, capacity, K, I, w1_fp4, w1_sf, gs_w1_gate,
+                        gs_w1_up, epilogue, out_bf16, epilogue == MOE_L1_SILU_BF16 ? h_amax : nullptr, h_fp4, h_sf,
+                        gs_h, dev_status, stream);
+}
+
+moe_status moe_requant(const void* h, int64_t capacity, int I, const int32_t* slot_token, const float* h_amax,
+                       float* gs_h_out, uint8_t* h_fp4, uint8_t* h_sf, int32_t* dev_status, moe_stream_t stream) {
+  if (!h || !slot_token || !h_amax || !gs_h_out || !h_fp4 || !h_sf || capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (I <= 0 || I % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(h, 16) || !aligned(h_fp4, 4) || !aligned(h_sf, 4)) return MOE_ERR_INVALID_ARG;
+  return quantize_launch(3, h, capacity, I, I, reinterpret_cast<const uint32_t*>(h_amax), nullptr, gs_h_out, h_fp4,
+                         h_sf, nullptr, 0, slot_token, capacity, dev_status, stream);
+}
+
+moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
+                               const int32_t* padded_offsets, int E, int64_t capacity, int I, int K,
+                               const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2, int epilogue,
+                               void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
+                               int64_t T, int32_t* dev_status, moe_stream_t stream) {
+  if (!h_fp4 || !h_sf || !gs_h || !offsets || !padded_offsets || !w2_fp4 || !w2_sf || !gs_w2)
+    return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(K, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (capacity <= 0 || capacity % kTileM || capacity > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (!aligned(h_fp4, 16) || !aligned(w2_fp4, 16) || !aligned(h_sf, 16) || !aligned(w2_sf, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (epilogue == MOE_L2_ROWS_BF16) {
+    if (!y_rows || !aligned(y_rows, 16)) return MOE_ERR_INVALID_ARG;
+  } else if (epilogue == MOE_L2_SCATTER) {
+    if (!slot_token || !slot_weight || !out32 || T < 0 || !aligned(out32, 16)) return MOE_ERR_INVALID_ARG;
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  return launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, capacity, I, K, w2_fp4, w2_sf, gs_w2,
+                        epilogue, y_rows, slot_token, slot_weight, out32, T, dev_status, stream);
+}
+
+moe_status moe_cast_output(const float* out32, void* out_bf16, int64_t T, int K, moe_stream_t stream) {
+  if (T < 0 || K <= 0 || K % 8) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!out32 || !out_bf16 || !aligned(out32, 16) || !aligned(out_bf16, 16)) return MOE_ERR_INVALID_ARG;
+  const int64_t n8 = T * K / 8;
+  const int blocks = (int)std::min<int64_t>(ceil_div(n8, 256), (int64_t)sm_count() * 8);
+  return launch_cast(out32, out_bf16, n8, blocks, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_forward(const void* x, int64_t T, int K, int I, int E, const int32_t* topk_ids, const float* topk_w,
+                       int topk, int expert_offset, const moe_weights* w, const float* gs_x_fixed, int gs_h_mode,
+                       float* gs_h, void* out, int32_t* dev_status, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  if (T < 0 || !w || !gs_h || !ws) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(K, I, E) || topk < 1 || topk > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!x || !topk_ids || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
+  if (gs_h_mode != MOE_GS_DYNAMIC && gs_h_mode != MOE_GS_FIXED) return MOE_ERR_INVALID_ARG;
+  if (!w->w1_fp4 || !w->w1_sf || !w->gs_w1_gate || !w->gs_w1_up || !w->w2_fp4 || !w->w2_sf || !w->gs_w2)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_workspace_size(T, K, I, E, topk)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+
+  Carve c{reinterpret_cast<uint8_t*>(ws)};
+  void* parts[14];
+  forward_layout(c, T, K, I, E, topk, parts);
+  const int64_t cap = moe_slot_capacity(T, topk, E);
+  uint32_t* scal = reinterpret_cast<uint32_t*>(parts[0]);
+  uint32_t* x_amax = scal + 0;
+  float* h_amax = reinterpret_cast<float*>(scal + 1);
+  float* gs_x = reinterpret_cast<float*>(scal + 2);
+  const size_t rhalf = moe_route_workspace_size(T, topk, E) / 2;
+  int32_t* rcnt = reinterpret_cast<int32_t*>(parts[1]);
+  int32_t* rbase = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(parts[1]) + rhalf);
+  int32_t* counts = reinterpret_cast<int32_t*>(parts[2]);
+  int32_t* offsets = reinterpret_cast<int32_t*>(parts[3]);
+  int32_t* poff = reinterpret_cast<int32_t*>(parts[4]);
+  int32_t* slot_token = reinterpret_cast<int32_t*>(parts[5]);
+  float* slot_weight = reinterpret_cast<float*>(parts[6]);
+  int32_t* pair_slot = reinterpret_cast<int32_t*>(parts[7]);
+  uint8_t* a_fp4 = reinterpret_cast<uint8_t*>(parts[8]);
+  uint8_t* a_sf = reinterpret_cast<uint8_t*>(parts[9]);
+  void* h_bf16 = parts[10];
+  uint8_t* h_fp4 = reinterpret_cast<uint8_t*>(parts[11]);
+  uint8_t* h_sf = reinterpret_cast<uint8_t*>(parts[12]);
+  float* out32 = reinterpret_cast<float*>(parts[13]);
+
+  moe_status s;
+  if (cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  s = route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, poff, slot_token, slot_weight,
+                 pair_slot, cap, rcnt, rbase, dev_status, stream);
+  if (s != MOE_OK) return s;
+  if (!gs_x_fixed) {
+    s = amax_launch(x, T, K, K, x_amax, stream);
+    if (s != MOE_OK) return s;
+  }
+  s = quantize_launch(2, x, T, K, K, gs_x_fixed ? nullptr : x_amax, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk,
+                      nullptr, cap, dev_status, stream);
+  if (s != MOE_OK) return s;
+  if (gs_h_mode == MOE_GS_DYNAMIC) {
+    s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
+                       w->gs_w1_up, MOE_L1_SILU_BF16, h_bf16, h_amax, nullptr, nullptr, nullptr, dev_status, stream);
+    if (s != MOE_OK) return s;
+    s = quantize_launch(3, h_bf16, cap, I, I, reinterpret_cast<const uint32_t*>(h_amax), nullptr, gs_h, h_fp4, h_sf,
+                        nullptr, 0, slot_token, cap, dev_status, stream);
+  } else {
+    s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
+                       w->gs_w1_up, MOE_L1_SILU_REQUANT, nullptr, nullptr, h_fp4, h_sf, gs_h, dev_status, stream);
+  }
+  if (s != MOE_OK) return s;
+  s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2, MOE_L2_SCATTER,
+                     nullptr, slot_token, slot_weight, out32, T, dev_status, stream);
+  if (s != MOE_OK) return s;
+  return moe_cast_output(out32, out, T, K, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,620 @@
+// Persistent grouped NVFP4 x NVFP4 GEMM on tcgen05 block-scaled MMA (sm_103a).
+//
+// Method: nvfp4-megamoe-kernel commits of src/nvfp4_megamoe_kernel/nvfp4_mega_moe.py
+// ("global scale as alpha": D = alpha * A @ B per expert, alpha = product of the
+// global scales), of src ("grouped GEMM over 1-D slot ranges"; the scale-factor
+// atom layout m = f0 + 32 f1 + 128 f2, k_sf = f4 + 4 f5), of vllm/nvfp4_cutedsl.py
+// ("intermediate_size": gate | up split at I; int32 expert offsets) and of tests
+// ("complete pipeline": SiLU(gate)*up in BF16, requantise, weighted scatter).
+//
+// Structure (one CTA per SM, 6 warps):
+//   warp 0      TMA producer: A tile (128 slot rows x 128 B = 256 fp4 of K), B tile
+//               (128 weight rows; for L1 64 gate rows + the matching 64 up rows),
+//               and the 4 scale atoms of each operand for the same K range, into a
+//               6-stage shared-memory ring guarded by full/empty mbarriers.
+//   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp moves the scale
+//               atoms into TMEM (32x128b, replicated to the 4 lane quarters), then
+//               four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128,
+//               N=128, K=64) accumulate fp32 into one of two TMEM accumulators.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows (one row per thread),
+//               alpha, BF16 rounding, and the fused per-layer tail (SiLU*up and
+//               requantisation for L1, weighted fp32 scatter-add for L2), while the
+//               MMA warp fills the other accumulator.
+// Tiles are (expert, n-tile, m-tile) with the m-tiles of one weight block adjacent,
+// so CTAs running at the same time share weight tiles through L2; the expert of a
+// tile comes from the padded offsets on the device (no host sync).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kBKBytes = 128;               // 256 fp4 per row per stage
+constexpr int kStages = 6;
+constexpr int kAStage = kBM * kBKBytes;     // 16 KB
+constexpr int kBStage = kBN * kBKBytes;     // 16 KB
+constexpr int kSfStage = 4 * 512;           // 4 scale atoms
+constexpr int kGemmThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kSfTmemBase = 256;            // stage s scales at 256 + 32 s (A: +0, B: +16)
+
+enum GemmKind : int { kL1GateUp = 0, kL1Silu = 1, kL1Requant = 2, kL2Rows = 3, kL2Scatter = 4 };
+
+struct GemmParams {
+  const uint8_t* a_sf;              // swizzled [cap/128][Kred/64][512]
+  const uint8_t* b_sf;              // prepared [E][rows_per_expert/128][Kred/64][512]
+  const int32_t* offsets;           // [E+1]
+  const int32_t* padded_offsets;    // [E+1]
+  int E;
+  int Kred;                         // contraction length in elements
+  int n_tiles;                      // output tiles per expert
+  int b_rows;                       // weight rows per expert
+  int I;                            // L1: columns of gate (= of up)
+  const float* gs_a;
+  const float* gs_b0;               // L1 gate / L2 down
+  const float* gs_b1;               // L1 up
+  void* out_bf16;
+  int64_t out_ld;                   // elements per output row
+  float* h_amax;
+  uint8_t* h_fp4;
+  uint8_t* h_sf;
+  const float* gs_h;
+  const int32_t* slot_token;
+  const float* slot_weight;
+  float* out32;
+  int64_t T;
+  int out_cols;                     // L2: K
+  int64_t cap;                      // slot rows of A (bound for the offsets)
+  int32_t* status;
+};
+
+struct __align__(1024) GemmSmem {
+  uint8_t a[kStages][kAStage];
+  uint8_t b[kStages][kBStage];
+  uint8_t sfa[kStages][kSfStage];
+  uint8_t sfb[kStages][kSfStage];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int bad_offsets;
+  int poff[257];
+  int cnt[256];
+};
+
+// ----------------------------------------------------------------------------- PTX
+MOE_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+MOE_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+MOE_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+MOE_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+MOE_DEV void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+MOE_DEV void tc_mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane; the wait sits in the same
+// asm statement so no use of the outputs can be scheduled before it.
+MOE_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B, 8-row
+// groups 1024 B apart (SBO), descriptor version 1, swizzle mode 2 (128B).
+MOE_DEV uint64_t sdesc_sw128(const void* p) {
+  const uint64_t addr = smem_u32(p);
+  return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+// Descriptor of one 512-byte scale atom seen as 32 rows x 16 B, no swizzle.
+MOE_DEV uint64_t sdesc_sf(const void* p) {
+  const uint64_t addr = smem_u32(p);
+  return ((addr & 0x3FFFFull) >> 4) | ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
+}
+// Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), K-major, UE4M3
+// scales (scale format 0), scale-factor ids 0, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+// Bounded wait: false on timeout (sets the abort flag and the status word) or when
+// another role already aborted.
+MOE_DEV bool wait_bar(uint64_t* bar, uint32_t parity, GemmSmem& s, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 255u) == 0) {
+      if (*(volatile int*)&s.abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *(volatile int*)&s.abort_flag = 1;
+        set_status(status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Tile t -> (expert, n-tile, m-tile); e advances monotonically with t.
+struct TileCursor {
+  int e = 0;
+  MOE_DEV bool locate(const GemmSmem& s, int E, int n_tiles, int t, int& n, int& m) {
+    while (e < E && t >= (s.poff[e + 1] >> 7) * n_tiles) ++e;
+    if (e >= E) return false;
+    const int tl = t - (s.poff[e] >> 7) * n_tiles;
+    const int mt = (s.poff[e + 1] - s.poff[e]) >> 7;
+    n = tl / mt;
+    m = tl - n * mt;
+    return true;
+  }
+};
+
+MOE_DEV float silu_mul(float g, float u) {
+  const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  return round_bf16(__fmul_rn(s, u));
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                        const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  GemmSmem& s = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr bool kL1 = KIND <= kL1Requant;
+
+  if (threadIdx.x == 0) s.bad_offsets = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.poff[i] = p.padded_offsets[i];
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s.cnt[i] = p.offsets[i + 1] - p.offsets[i];
+  __syncthreads();
+  // the tile walk trusts the offsets: check them once (monotone, 128-aligned,
+  // counts within their padded ranges, inside the slot capacity)
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
+    const int lo = s.poff[i], hi = s.poff[i + 1], c = s.cnt[i];
+    if (lo < 0 || hi < lo || (lo & 127) || (hi & 127) || c < 0 || c > hi - lo || hi > p.cap)
+      s.bad_offsets = 1;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  const bool bad = s.bad_offsets != 0;
+  if (bad && threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE_INDEX);
+  const int total_tiles = bad ? 0 : (s.poff[p.E] >> 7) * p.n_tiles;
+  const int nkb = (p.Kred + 255) >> 8;
+  const int ksf4 = p.Kred >> 6;  // scale atoms per 128 rows
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[kStages];
+      bool issued[kStages];
+      for (int i = 0; i < kStages; ++i) issued[i] = false;
+      bool ok = true;
+      TileCursor cur;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        int n, m;
+        if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
+        const int e = cur.e;
+        const int row_a = s.poff[e] + m * kBM;
+        const uint8_t* sfa_src = p.a_sf + ((int64_t)(row_a >> 7) * ksf4) * 512;
+        const uint8_t* sfb_src =
+            p.b_sf + ((int64_t)e * (p.b_rows >> 7) + n) * (int64_t)ksf4 * 512;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int natoms = min(4, ksf4 - 4 * kb);
+          if (!wait_bar(&s.empty[stage], phase ^ 1, s, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.full[stage], kAStage + kBStage + 2 * natoms * 512);
+          const int x = kb * kBKBytes;
+          tma_load_2d(s.a[stage], &tmap_a, &s.full[stage], x, row_a);
+          if (kL1) {
+            const int yb = e * p.b_rows + n * 64;
+            tma_load_2d(s.b[stage], &tmap_b, &s.full[stage], x, yb);
+            tma_load_2d(s.b[stage] + kBStage / 2, &tmap_b, &s.full[stage], x, yb + p.I);
+          } else {
+            tma_load_2d(s.b[stage], &tmap_b, &s.full[stage], x, e * p.b_rows + n * kBN);
+          }
+          bulk_load(s.sfa[stage], sfa_src + kb * 4 * 512, natoms * 512, &s.full[stage]);
+          bulk_load(s.sfb[stage], sfb_src + kb * 4 * 512, natoms * 512, &s.full[stage]);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok || *(volatile int*)&s.abort_flag) {
+        // let copies already in flight land before the CTA's shared memory goes away
+        for (int i = 0; i < kStages; ++i)
+          if (issued[i]) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&s.full[i], issued_phase[i]) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      TileCursor cur;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++it) {
+        int n, m;
+        if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
+        const int acc = it & 1;
+        if (!wait_bar(&s.tempty[acc], ((it >> 1) & 1) ^ 1, s, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * kBN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int natoms = min(4, ksf4 - 4 * kb);
+          if (!wait_bar(&s.full[stage], phase, s, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sf_col = tmem + kSfTmemBase + 32 * stage;
+          for (int a = 0; a < natoms; ++a) {
+            tc_cp_sf(sf_col + 4 * a, sdesc_sf(s.sfa[stage] + 512 * a));
+            tc_cp_sf(sf_col + 16 + 4 * a, sdesc_sf(s.sfb[stage] + 512 * a));
+          }
+          for (int kk = 0; kk < natoms; ++kk) {
+            tc_mma_fp4(d, sdesc_sw128(s.a[stage] + 32 * kk), sdesc_sw128(s.b[stage] + 32 * kk), kIdesc,
+                       sf_col + 4 * kk, sf_col + 16 + 4 * kk, (kb | kk) != 0);
+          }
+          tc_commit(&s.empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&s.tfull[acc]);
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      tc_commit(&s.drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&s.drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int it = 0;
+    TileCursor cur;
+    float amax = 0.0f;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      int n, m;
+      if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
+      const int e = cur.e;
+      const int acc = it & 1;
+      if (!wait_bar(&s.tfull[acc], (it >> 1) & 1, s, p.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kBN;
+      const bool valid = m * kBM + row < s.cnt[e];
+      const int64_t prow = (int64_t)s.poff[e] + m * kBM + row;
+      if (kL1) {
+        const float gs_a = __ldg(p.gs_a);
+        const float ag = __fmul_rn(gs_a, __ldg(p.gs_b0 + e));
+        const float au = __fmul_rn(gs_a, __ldg(p.gs_b1 + e));
+        float rg = 0.0f;
+        if (KIND == kL1Requant) rg = recip_global_scale(__ldg(p.gs_h));
+        uint32_t sfw = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float g[16], u[16];
+          tmem_ld16(taddr + c * 16, g);
+          tmem_ld16(taddr + 64 + c * 16, u);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            g[i] = round_bf16(__fmul_rn(ag, g[i]));
+            u[i] = round_bf16(__fmul_rn(au, u[i]));
+          }
+          const int col = n * 64 + c * 16;  // h column (gate/up column) of element 0
+          if (KIND == kL1GateUp) {
+            if (valid) {
+              uint4* dg = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
+              uint4* du = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + p.I + col);
+              dg[0] = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
+              dg[1] = make_uint4(pack_bf16x2(g[8], g[9]), pack_bf16x2(g[10], g[11]), pack_bf16x2(g[12], g[13]), pack_bf16x2(g[14], g[15]));
+              du[0] = make_uint4(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]), pack_bf16x2(u[4], u[5]), pack_bf16x2(u[6], u[7]));
+              du[1] = make_uint4(pack_bf16x2(u[8], u[9]), pack_bf16x2(u[10], u[11]), pack_bf16x2(u[12], u[13]), pack_bf16x2(u[14], u[15]));
+            }
+          } else {
+            float h[16];
+            float bm = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              h[i] = silu_mul(g[i], u[i]);
+              bm = fmaxf(bm, fabsf(h[i]));
+            }
+            if (valid) {
+              if (p.out_bf16) {
+                uint4* dh = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
+                dh[0] = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+                dh[1] = make_uint4(pack_bf16x2(h[8], h[9]), pack_bf16x2(h[10], h[11]), pack_bf16x2(h[12], h[13]), pack_bf16x2(h[14], h[15]));
+              }
+              amax = fmaxf(amax, bm);
+            }
+            if (KIND == kL1Requant) {
+              float rb;
+              const uint32_t sb = block_scale(bm, rg, rb);
+              uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t b0 = e2m1x2(code_mag(fabsf(h[2 * i]), rg, rb), code_mag(fabsf(h[2 * i + 1]), rg, rb)) |
+                              sign_bits2(h[2 * i], h[2 * i + 1]);
+                uint32_t b1 = e2m1x2(code_mag(fabsf(h[8 + 2 * i]), rg, rb), code_mag(fabsf(h[8 + 2 * i + 1]), rg, rb)) |
+                              sign_bits2(h[8 + 2 * i], h[8 + 2 * i + 1]);
+                w0 |= b0 << (8 * i);
+                w1 |= b1 << (8 * i);
+              }
+              sfw |= sb << (8 * c);
+              if (valid)
+                *reinterpret_cast<uint2*>(p.h_fp4 + prow * (p.I >> 1) + (col >> 1)) = make_uint2(w0, w1);
+            }
+          }
+        }
+        if (KIND == kL1Requant && valid)
+          *reinterpret_cast<uint32_t*>(p.h_sf + sf_swizzle_offset(prow, n * 4, p.I >> 4)) = sfw;
+      } else {
+        const float alpha = __fmul_rn(__ldg(p.gs_a), __ldg(p.gs_b0 + e));
+        int32_t tok = -1;
+        float wgt = 0.0f;
+        if (KIND == kL2Scatter && valid) {
+          tok = __ldg(p.slot_token + prow);
+          wgt = __ldg(p.slot_weight + prow);
+          if (tok >= p.T) { set_status(p.status, MOE_ERR_DEVICE_INDEX); tok = -1; }
+        }
+#pragma unroll 1
+        for (int c = 0; c < kBN / 16; ++c) {
+          float y[16];
+          tmem_ld16(taddr + c * 16, y);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = round_bf16(__fmul_rn(alpha, y[i]));
+          const int col = n * kBN + c * 16;
+          if (KIND == kL2Rows) {
+            if (valid) {
+              uint4* dy = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
+              dy[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+              dy[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]), pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
+            }
+          } else if (tok >= 0) {
+            float4* dst = reinterpret_cast<float4*>(p.out32 + (int64_t)tok * p.out_cols + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              atomicAdd(dst + j, make_float4(__fmul_rn(wgt, y[4 * j]), __fmul_rn(wgt, y[4 * j + 1]),
+                                             __fmul_rn(wgt, y[4 * j + 2]), __fmul_rn(wgt, y[4 * j + 3])));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[acc]);
+    }
+    if (KIND == kL1Silu && p.h_amax) {
+      // non-negative floats order like their bit patterns
+      const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
+      if (lane == 0 && mb) atomicMax(reinterpret_cast<uint32_t*>(p.h_amax), mb);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ----------------------------------------------------------------------------- host
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// Row-major byte matrix [rows, row_bytes] as a 2-D uint8 tensor map with a
+// 128-byte-swizzled box of box_rows x 128 B.
+static bool make_tmap(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)kBKBytes, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return n;
+}
+
+constexpr size_t kGemmSmemBytes = sizeof(GemmSmem) + 1024;
+
+template <int KIND>
+static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGemmSmemBytes) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured = true;
+  }
+  grouped_gemm_kernel<KIND><<<num_sms(), kGemmThreads, kGemmSmemBytes, st>>>(ta, tb, p);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// L1: A = slot activations [cap, K/2]; B = W1 [E*2I, K/2]; N per tile = 64 h cols.
+moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,
+                          const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
+                          const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
+                          float* h_amax, uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h, int32_t* status,
+                          cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tb, w1_fp4, (uint64_t)K / 2, (uint64_t)E * 2 * I, 64)) return MOE_ERR_CUDA;
+  GemmParams p{};
+  p.a_sf = a_sf;
+  p.b_sf = w1_sf;
+  p.offsets = offsets;
+  p.padded_offsets = padded_offsets;
+  p.E = E;
+  p.Kred = K;
+  p.n_tiles = I / 64;
+  p.b_rows = 2 * I;
+  p.I = I;
+  p.cap = cap;
+  p.gs_a = gs_a;
+  p.gs_b0 = gs_g;
+  p.gs_b1 = gs_u;
+  p.out_bf16 = out_bf16;
+  p.out_ld = epilogue == MOE_L1_GATEUP_BF16 ? 2 * (int64_t)I : I;
+  p.h_amax = h_amax;
+  p.h_fp4 = h_fp4;
+  p.h_sf = h_sf;
+  p.gs_h = gs_h;
+  p.status = status;
+  if (epilogue == MOE_L1_SILU_BF16 && h_amax && cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  switch (epilogue) {
+    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, p, st);
+    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, p, st);
+    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(ta, tb, p, st);
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+// L2: A = h codes [cap, I/2]; B = W2 [E*K, I/2]; N per tile = 128 output cols.
+moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
+                          const int32_t* padded_offsets, int E, int64_t cap, int I, int K, const uint8_t* w2_fp4,
+                          const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
+                          const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
+                          int32_t* status, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tb, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, kBN)) return MOE_ERR_CUDA;
+  GemmParams p{};
+  p.a_sf = h_sf;
+  p.b_sf = w2_sf;
+  p.offsets = offsets;
+  p.padded_offsets = padded_offsets;
+  p.E = E;
+  p.Kred = I;
+  p.n_tiles = K / kBN;
+  p.b_rows = K;
+  p.I = I;
+  p.gs_a = gs_h;
+  p.gs_b0 = gs_w2;
+  p.out_bf16 = y_rows;
+  p.out_ld = K;
+  p.slot_token = slot_token;
+  p.slot_weight = slot_weight;
+  p.out32 = out32;
+  p.T = T;
+  p.out_cols = K;
+  p.cap = cap;
+  p.status = status;
+  switch (epilogue) {
+    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, p, st);
+    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, p, st);
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+}  // namespace moe

@@ -1,0 +1,63 @@
+// Declarations shared between the kernel translation units and the C ABI layer.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---- quant.cu ----
+enum QuantDst : int {
+  kDstRowMajorSf = 0,  // codes [rows, K/2], scales [rows, K/16]
+  kDstSwizzledSf = 1,  // codes [rows, K/2], scales swizzled
+  kDstSlots = 2,       // row t -> slots pair_slot[t*topk + j] (swizzled scales)
+  kDstMasked = 3,      // row r written iff slot_token[r] >= 0 (swizzled scales)
+};
+
+struct QuantArgs {
+  const uint4* x;             // rows of bf16, 16-byte vectors
+  int64_t rows;
+  int K;                      // elements per row (multiple of 64)
+  int64_t ld_vec;             // row stride in 16-byte vectors
+  const uint32_t* amax_bits;  // dynamic: fp32 bits of max|x|  (or NULL)
+  const float* gs_fixed;      // fixed global scale (or NULL)
+  float* gs_out;              // written by one thread (or NULL)
+  uint8_t* codes;
+  uint8_t* sf;
+  const int32_t* pair_slot;   // kDstSlots
+  int topk;
+  const int32_t* slot_token;  // kDstMasked
+  int64_t capacity;           // kDstSlots: bound on slot indices
+  int32_t* status;
+};
+
+// Host launchers (each translation unit launches its own kernels).
+cudaError_t launch_amax(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, int blocks,
+                        cudaStream_t st);
+cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st);
+cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st);
+cudaError_t launch_prepare_weight_sf(const uint8_t* src, uint8_t* dst, int E, int N, int k_sf, int gateup,
+                                     int blocks, cudaStream_t st);
+
+// ---- route.cu ----
+constexpr int kRouteChunk = 256;  // pairs per warp
+constexpr int kRouteWarps = 8;    // warps per block (count / place)
+constexpr int kMaxExperts = 256;
+
+cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk, int E, int off, int32_t* cnt,
+                         int32_t* base, int nchunks, int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                         int32_t* slot_token, float* slot_weight, int32_t* pair_slot, int64_t capacity,
+                         int32_t* status, cudaStream_t st);
+
+// ---- gemm.cu ----
+moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,
+                          const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
+                          const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
+                          float* h_amax, uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h, int32_t* status,
+                          cudaStream_t st);
+moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
+                          const int32_t* padded_offsets, int E, int64_t cap, int I, int K, const uint8_t* w2_fp4,
+                          const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
+                          const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
+                          int32_t* status, cudaStream_t st);
+
+}  // namespace moe

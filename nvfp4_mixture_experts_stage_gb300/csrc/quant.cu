@@ -1,0 +1,226 @@
+// NVFP4 quantisation kernels: global amax, block quantisation (row-major,
+// swizzled, into slot rows, or of masked slot rows), output cast and the
+// one-time weight-scale rearrangement.
+//
+// Method: nvfp4-megamoe-kernel commits of src/nvfp4_megamoe_kernel/nvfp4_mega_moe.py
+// ("three bugs fixed" commit: sign-magnitude E2M1 nibbles, scale = block_max/6;
+// "global scale" commit: gs = amax/(6*448) normalises before blocking), commits of
+// tests ("float4_e2m1fn_x2": two codes per byte along K) and of src (the
+// scale-factor atom layout of the block-scaled MMA).
+//
+// Data movement: one warp owns a 256-element segment of a row per step; lane l
+// holds elements [8l, 8l+8) as one 16-byte load, so lanes (2i, 2i+1) form the
+// 16-element block i and the warp's loads and code stores are fully coalesced
+// (512 B in, 128 B out).  Four consecutive block scales of a row are assembled
+// into one 32-bit store by lane 8j (they are contiguous in both scale layouts).
+#include "kernels.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// max |x| over a BF16 matrix -> fp32 bits, atomically max-ed into *amax_bits
+// (must hold 0 or a previous non-negative value on entry).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) amax_bf16_kernel(const uint4* __restrict__ x, int64_t T,
+                                                        int vec_per_row, int64_t ld_vec,
+                                                        uint32_t* amax_bits) {
+  // vector index v -> (row, column); 32-bit division (the host keeps T*vec_per_row < 2^32)
+  const uint32_t total = (uint32_t)(T * vec_per_row);
+  const uint32_t vpr = (uint32_t)vec_per_row;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  auto addr = [&](uint32_t v) {
+    const uint32_t r = v / vpr;
+    return x + (int64_t)r * ld_vec + (v - r * vpr);
+  };
+  uint32_t m = 0;
+  uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  // 4 independent loads in flight per thread
+  for (; i + 3 * stride < total; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(addr(i + u * stride));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      m = __vmaxu2(m, v[u].x & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].y & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].z & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].w & 0x7FFF7FFFu);
+    }
+  }
+  for (; i < total; i += stride) {
+    const uint4 v = __ldg(addr(i));
+    m = __vmaxu2(m, v.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+  }
+  // bf16 magnitude bits order like the magnitudes (non-NaN inputs)
+  m = max(m & 0xFFFFu, m >> 16);
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (threadIdx.x == 0 && v) atomicMax(amax_bits, v << 16);  // bf16 -> fp32 bits
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Block quantisation.
+// ---------------------------------------------------------------------------
+template <int DST>
+__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
+  const float gs = a.gs_fixed ? __ldg(a.gs_fixed)
+                              : __fdiv_rn(__uint_as_float(*a.amax_bits), kGsDivisor);
+  const float rg = recip_global_scale(gs);
+  if (a.gs_out && blockIdx.x == 0 && threadIdx.x == 0) *a.gs_out = gs;
+
+  const int lane = threadIdx.x & 31;
+  // segment index s -> (row, segment); 32-bit (the host keeps rows*nseg < 2^31)
+  const uint32_t nseg = (uint32_t)((a.K + 255) >> 8);
+  const uint32_t total = (uint32_t)(a.rows * nseg);
+  const uint32_t warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int k_sf = a.K >> 4;
+  const int half_k = a.K >> 1;
+
+  constexpr int U = 4;
+  for (uint32_t base = warp0; base < total; base += nwarps * U) {
+    uint4 v[U];
+    int64_t row[U];
+    int col[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t s = base + u * nwarps;
+      const uint32_t r = s / nseg;
+      row[u] = r;
+      col[u] = (int)(s - r * nseg) * 256 + lane * 8;  // first element of this lane
+      bool ok = s < total && col[u] < a.K;
+      if (ok && DST == kDstMasked) ok = __ldg(a.slot_token + row[u]) >= 0;
+      v[u] = ok ? __ldcs(a.x + row[u] * a.ld_vec + (col[u] >> 3)) : make_uint4(0, 0, 0, 0);
+      if (!ok) col[u] = -1;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(w[i]); f[2 * i + 1] = bf16hi(w[i]); }
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+      const float bm = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      float rb;
+      const uint32_t sb = block_scale(bm, rg, rb);
+      uint32_t code = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = f[2 * i], hi = f[2 * i + 1];
+        uint32_t byte = e2m1x2(code_mag(fabsf(lo), rg, rb), code_mag(fabsf(hi), rg, rb));
+        byte |= sign_bits2(lo, hi);
+        code |= byte << (8 * i);
+      }
+      // scale word of 4 blocks, assembled on lane 8j from lanes 8j, 8j+2, 8j+4, 8j+6
+      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
+      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
+      const uint32_t sfw = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      if (col[u] < 0) continue;
+      const bool sf_lane = (lane & 7) == 0;
+      const int ks = col[u] >> 4;  // scale column of this lane's block
+      if (DST == kDstSlots) {
+        for (int j = 0; j < a.topk; ++j) {
+          const int32_t p = __ldg(a.pair_slot + row[u] * a.topk + j);
+          if (p < 0) continue;
+          if (p >= a.capacity) { set_status(a.status, MOE_ERR_DEVICE_INDEX); continue; }
+          *reinterpret_cast<uint32_t*>(a.codes + (int64_t)p * half_k + (col[u] >> 1)) = code;
+          if (sf_lane)
+            *reinterpret_cast<uint32_t*>(a.sf + sf_swizzle_offset(p, ks, k_sf)) = sfw;
+        }
+      } else {
+        *reinterpret_cast<uint32_t*>(a.codes + row[u] * half_k + (col[u] >> 1)) = code;
+        if (sf_lane) {
+          const int64_t off = (DST == kDstRowMajorSf) ? row[u] * k_sf + ks
+                                                      : sf_swizzle_offset(row[u], ks, k_sf);
+          *reinterpret_cast<uint32_t*>(a.sf + off) = sfw;
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st) {
+  switch (dst) {
+    case kDstRowMajorSf: quantize_kernel<kDstRowMajorSf><<<blocks, 256, 0, st>>>(a); break;
+    case kDstSwizzledSf: quantize_kernel<kDstSwizzledSf><<<blocks, 256, 0, st>>>(a); break;
+    case kDstSlots: quantize_kernel<kDstSlots><<<blocks, 256, 0, st>>>(a); break;
+    default: quantize_kernel<kDstMasked><<<blocks, 256, 0, st>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, int blocks,
+                        cudaStream_t st) {
+  amax_bf16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), rows, K / 8, ld_x / 8, amax_bits);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// out_bf16 = bf16(out32), 8 elements per thread.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) cast_f32_bf16_kernel(const float4* __restrict__ in,
+                                                            uint4* __restrict__ out, int64_t n8) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = __ldcs(in + 2 * i), b = __ldcs(in + 2 * i + 1);
+    uint4 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    o.z = pack_bf16x2(b.x, b.y);
+    o.w = pack_bf16x2(b.z, b.w);
+    __stcs(out + i, o);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Weight scales [E, N, K_sf] row-major -> the GEMM's layout (setup only).
+// gateup: logical row r of W1 (gate 0..I-1, up I..2I-1) goes to row
+// 128*(r'/64) + (r'%64) (+64 for up), r' = r mod I, so each 128-row atom
+// holds 64 gate rows then the matching 64 up rows.
+// ---------------------------------------------------------------------------
+__global__ void prepare_weight_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                         int E, int N, int k_sf, int gateup) {
+  const int64_t per = (int64_t)N * k_sf;
+  const int64_t total = (int64_t)E * per;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int I = N / 2;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t e = i / per;
+    const int64_t rem = i - e * per;
+    const int r = (int)(rem / k_sf);
+    const int k = (int)(rem - (int64_t)r * k_sf);
+    int m = r;
+    if (gateup) {
+      const int up = r >= I;
+      const int rr = up ? r - I : r;
+      m = (rr >> 6) * 128 + up * 64 + (rr & 63);
+    }
+    dst[e * per + sf_swizzle_offset(m, k, k_sf)] = src[i];
+  }
+}
+
+cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st) {
+  cast_f32_bf16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), reinterpret_cast<uint4*>(out),
+                                              n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_weight_sf(const uint8_t* src, uint8_t* dst, int E, int N, int k_sf, int gateup,
+                                     int blocks, cudaStream_t st) {
+  prepare_weight_sf_kernel<<<blocks, 256, 0, st>>>(src, dst, E, N, k_sf, gateup);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

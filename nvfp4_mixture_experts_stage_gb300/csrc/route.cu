@@ -1,0 +1,154 @@
+// Token -> slot routing on the device, with no host synchronisation.
+//
+// Method: nvfp4-megamoe-kernel commits of src/nvfp4_megamoe_kernel/nvfp4_mega_moe.py
+// ("global expert ids": subtract the rank's first expert id, drop foreign ids),
+// of src ("1-D slot_expert_ids / slot_token"), of vllm/nvfp4_cutedsl.py ("CUDA
+// graph" commits: sort pairs by expert, bincount + cumsum int32 offsets on the
+// device, zero-weight padding) and of tests ("token layout": rows grouped
+// [expert 0 | expert 1 | ...]).
+//
+// Three launches over chunks of 256 (token, k) pairs, one chunk per warp:
+//   count: warp-level histogram (__match_any_sync groups equal experts, the
+//          group leader adds the group size) -> cnt[e][chunk];
+//   scan:  one block; per expert a warp-level prefix sum over chunks gives each
+//          chunk's first rank, then a scan over experts gives offsets and
+//          128-padded offsets;
+//   place: each warp walks its chunk again in order, ranks pairs within the
+//          32-pair group by popcount of the lower lanes of its match group, and
+//          writes slot_token / slot_weight / pair_slot.
+// Processing every chunk in order and every group in lane order makes the
+// placement stable: slots of an expert follow ascending t*topk + j.
+#include "kernels.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ int local_expert(const int32_t* ids, int64_t idx, int64_t P, int off, int E) {
+  if (idx >= P) return -1;
+  const int l = __ldg(ids + idx) - off;
+  return (l >= 0 && l < E) ? l : -1;
+}
+
+__global__ void __launch_bounds__(kRouteWarps * 32) route_count_kernel(
+    const int32_t* __restrict__ ids, int64_t P, int E, int off, int32_t* __restrict__ cnt, int nchunks) {
+  __shared__ int hist[kRouteWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kRouteWarps + warp;
+  if (chunk >= nchunks) return;  // whole warp leaves together
+  for (int e = lane; e < E; e += 32) hist[warp][e] = 0;
+  __syncwarp();
+  const int64_t base = (int64_t)chunk * kRouteChunk;
+  int loc[kRouteChunk / 32];
+#pragma unroll
+  for (int g = 0; g < kRouteChunk / 32; ++g) loc[g] = local_expert(ids, base + g * 32 + lane, P, off, E);
+#pragma unroll
+  for (int g = 0; g < kRouteChunk / 32; ++g) {
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, loc[g]);
+    if (loc[g] >= 0 && lane == __ffs(grp) - 1) hist[warp][loc[g]] += __popc(grp);
+    __syncwarp();
+  }
+  for (int e = lane; e < E; e += 32) cnt[(int64_t)e * nchunks + chunk] = hist[warp][e];
+}
+
+// One block of 1024 threads.
+__global__ void __launch_bounds__(1024) route_scan_kernel(
+    const int32_t* __restrict__ cnt, int nchunks, int E, int32_t* __restrict__ base,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets) {
+  __shared__ int s_cnt[kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += 32) {
+    int running = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunks ? cnt[(int64_t)e * nchunks + c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += t;
+      }
+      if (c < nchunks) base[(int64_t)e * nchunks + c] = running + incl - v;
+      running += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) s_cnt[e] = running;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0, prun = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? s_cnt[e] : 0;
+      const int pv = (v + kTileM - 1) / kTileM * kTileM;
+      int incl = v, pincl = pv;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        const int pt = __shfl_up_sync(0xFFFFFFFFu, pincl, d);
+        if (lane >= d) { incl += t; pincl += pt; }
+      }
+      if (e < E) {
+        counts[e] = v;
+        offsets[e] = run + incl - v;
+        padded_offsets[e] = prun + pincl - pv;
+      }
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      prun += __shfl_sync(0xFFFFFFFFu, pincl, 31);
+    }
+    if (lane == 0) {
+      offsets[E] = run;
+      padded_offsets[E] = prun;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRouteWarps * 32) route_place_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t P, int topk, int E, int off,
+    const int32_t* __restrict__ base, int nchunks, const int32_t* __restrict__ padded_offsets,
+    int32_t* __restrict__ slot_token, float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot,
+    int64_t capacity, int32_t* status) {
+  __shared__ int run[kRouteWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kRouteWarps + warp;
+  if (chunk >= nchunks) return;
+  for (int e = lane; e < E; e += 32)
+    run[warp][e] = __ldg(padded_offsets + e) + base[(int64_t)e * nchunks + chunk];
+  __syncwarp();
+  const int64_t base_idx = (int64_t)chunk * kRouteChunk;
+  const unsigned lower = (1u << lane) - 1u;
+#pragma unroll 2
+  for (int g = 0; g < kRouteChunk / 32; ++g) {
+    const int64_t idx = base_idx + g * 32 + lane;
+    const int l = local_expert(ids, idx, P, off, E);
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, l);
+    int slot = -1;
+    if (l >= 0) slot = run[warp][l] + __popc(grp & lower);
+    __syncwarp();
+    if (l >= 0 && lane == __ffs(grp) - 1) run[warp][l] += __popc(grp);
+    __syncwarp();
+    if (idx < P) {
+      if (slot >= capacity) {
+        set_status(status, MOE_ERR_DEVICE_INDEX);
+        slot = -1;
+      }
+      pair_slot[idx] = slot;
+      if (slot >= 0) {
+        slot_token[slot] = (int32_t)(idx / topk);
+        slot_weight[slot] = __ldg(w + idx);
+      }
+    }
+  }
+}
+
+cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk, int E, int off, int32_t* cnt,
+                         int32_t* base, int nchunks, int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                         int32_t* slot_token, float* slot_weight, int32_t* pair_slot, int64_t capacity,
+                         int32_t* status, cudaStream_t st) {
+  const int blocks = (nchunks + kRouteWarps - 1) / kRouteWarps;
+  if (nchunks > 0) route_count_kernel<<<blocks, kRouteWarps * 32, 0, st>>>(ids, P, E, off, cnt, nchunks);
+  route_scan_kernel<<<1, 1024, 0, st>>>(cnt, nchunks, E, base, counts, offsets, padded_offsets);
+  if (nchunks > 0)
+    route_place_kernel<<<blocks, kRouteWarps * 32, 0, st>>>(ids, w, P, topk, E, off, base, nchunks, padded_offsets,
+                                                           slot_token, slot_weight, pair_slot, capacity, status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,75 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and its host-side logic (size queries, argument checks) behaves."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_stage.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from nvfp4_mixture_experts_stage_gb300 import build
+    build.build()
+    from nvfp4_mixture_experts_stage_gb300 import binding
+    return binding
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_are_all_exported(B):
+    names = _declared()
+    assert set(names) == set(B.EXPORTS)
+    for n in names:
+        assert hasattr(B.library(), n), n
+
+
+def test_status_strings(B):
+    for s in range(7):
+        assert B.moe_status_string(s)
+    assert "workspace" in B.moe_status_string(B.MOE_ERR_WORKSPACE)
+
+
+def test_slot_capacity(B):
+    assert B.moe_slot_capacity(16, 2, 8) == 1152           # 32 + 127*8 = 1048 -> 9*128
+    assert B.moe_slot_capacity(0, 1, 1) == 128
+    assert B.moe_slot_capacity(8192, 8, 48) % 128 == 0
+    assert B.moe_slot_capacity(8192, 8, 48) >= 8192 * 8 + 127 * 48
+    assert B.moe_slot_capacity(-1, 1, 1) == -1
+
+
+def test_workspace_sizes(B):
+    assert B.moe_stage_workspace_size() >= 4
+    assert B.moe_route_workspace_size(256, 8, 48) >= 2 * 8 * 48 * 4
+    small = B.moe_workspace_size(16, 256, 128, 8, 2)
+    big = B.moe_workspace_size(8192, 4096, 3072, 48, 8)
+    assert 0 < small < big
+    # unsupported shapes give 0
+    assert B.moe_workspace_size(16, 100, 128, 8, 2) == 0
+    assert B.moe_workspace_size(16, 256, 100, 8, 2) == 0
+    assert B.moe_workspace_size(16, 256, 128, 300, 2) == 0
+
+
+def test_argument_checks_fail_before_any_device_work(B):
+    lib = B.library()
+    null = ctypes.c_void_p(0)
+    # null pointers / bad enums / bad shapes are rejected on the host
+    assert lib.moe_route(null, null, 4, 2, 8, 0, null, null, null, null, null, null, 1024, null, 0, null) \
+        == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(null, null, 4, 64, 8, 0, null, null, null, null, null, null, 1024, null, 0, null) \
+        == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_prepare_weights(null, null, 1, 128, 64, 0, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_gemm_l1(null, null, null, null, null, 1, 128, 256, 128, null, null, null, null, 0,
+                                   null, null, null, null, null, null, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_cast_output(null, null, 4, 7, null) == B.MOE_ERR_INVALID_ARG
+    w = B.MoeWeights()
+    assert lib.moe_forward(null, 4, 256, 100, 8, null, null, 2, 0, ctypes.byref(w), null, 0, null, null, null,
+                           null, 0, null) in (B.MOE_ERR_INVALID_ARG, B.MOE_ERR_UNSUPPORTED_SHAPE)

@@ -1,0 +1,188 @@
+"""GPU parity of the quantiser and the router against the oracle: bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import nvfp4 as q
+from oracle.route import route as oroute
+from tests.helpers import bf16_dev
+
+pytestmark = pytest.mark.gpu
+
+B = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    global B
+    from nvfp4_mixture_experts_stage_gb300 import binding
+    B = binding
+
+
+def _stage(x_f32, layout, gs_fixed=None):
+    T, K = x_f32.shape
+    x = bf16_dev(x_f32)
+    codes = torch.zeros(T, K // 2, dtype=torch.uint8, device="cuda")
+    rows = -(-T // 128) * 128 if layout == 1 else T
+    sf = torch.zeros(rows * K // 16, dtype=torch.uint8, device="cuda")
+    gs = torch.zeros(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.moe_stage_workspace_size(), dtype=torch.uint8, device="cuda")
+    gfix = None if gs_fixed is None else torch.tensor([gs_fixed], dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_stage_activation(x, codes, sf, layout, gs, gs_fixed=gfix, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return codes.cpu().numpy(), sf.cpu().numpy(), np.float32(gs.item())
+
+
+def _rand_x(T, K, seed, scale=1.0, outliers=False):
+    r = np.random.default_rng(seed)
+    x = r.standard_normal((T, K)).astype(np.float32) * np.float32(scale)
+    if outliers:
+        x = np.where(r.random((T, K)) < 0.01, x * 20, x).astype(np.float32)
+    return q.bf16_round(x)
+
+
+@pytest.mark.parametrize("T,K,scale,outl", [(1, 64, 1.0, False), (7, 192, 1.0, True), (33, 320, 3.0, False),
+                                            (130, 4096, 1.0, True), (256, 7168, 1e4, False),
+                                            (5, 256, 1e-3, False), (64, 512, 1e30, False)])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_stage_activation_bit_exact(T, K, scale, outl, layout):
+    x = _rand_x(T, K, T * 1000 + K, scale, outl)
+    codes, sf, gs = _stage(x, layout)
+    rc, rs, rg = q.quantize(x)
+    assert gs == rg
+    assert np.array_equal(codes, rc)
+    if layout == 0:
+        assert np.array_equal(sf.reshape(T, K // 16), rs)
+    else:
+        assert np.array_equal(q.unswizzle(sf, T, K // 16), rs)
+
+
+@pytest.mark.parametrize("gs_fixed", [1.0, 0.5, 1e-3, 7.0 / 2688.0, 0.0, 1e-42])
+def test_stage_activation_fixed_scale_bit_exact(gs_fixed):
+    x = _rand_x(48, 256, 5, 2.0, True)
+    codes, sf, gs = _stage(x, 0, gs_fixed)
+    rc, rs, _ = q.quantize(x, np.float32(gs_fixed))
+    assert gs == np.float32(gs_fixed)
+    assert np.array_equal(codes, rc)
+    assert np.array_equal(sf.reshape(48, 16), rs)
+
+
+def test_stage_activation_ties_signs_and_golden_blocks():
+    # every E2M1 tie and grid point, both signs, with scale 1 (block max 6, gs 1)
+    vals = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0],
+                    np.float32)
+    rows = [vals, -vals, np.where(np.arange(16) % 2 == 0, -0.0, 0.0).astype(np.float32),
+            np.array([6.0] + [1e-6] * 15, np.float32), np.array([-6.0] + [-1e-6] * 15, np.float32)]
+    x = np.stack(rows).astype(np.float32)
+    x = np.tile(x, (1, 4))
+    codes, sf, gs = _stage(x, 0, 1.0)
+    rc, rs, _ = q.quantize(x, np.float32(1.0))
+    assert np.array_equal(codes, rc)
+    assert np.array_equal(sf.reshape(len(rows), 4), rs)
+    # -0.0 and tiny negatives code as 0x8 (sign bit kept)
+    assert np.all(q.unpack_nibbles(codes)[2, 0::2] == 8)
+
+
+def test_stage_activation_all_zero():
+    x = np.zeros((3, 64), np.float32)
+    codes, sf, gs = _stage(x, 0)
+    assert gs == 0.0 and not codes.any() and not sf.any()
+
+
+def _route_dev(ids, w, E, off):
+    T, k = ids.shape
+    cap = B.moe_slot_capacity(T, k, E)
+    d = lambda n, dt=torch.int32: torch.full((n,), -7, dtype=dt, device="cuda")
+    counts, offs, poff = d(E), d(E + 1), d(E + 1)
+    st, sw, ps = d(cap), d(cap, torch.float32), d(T * k)
+    ws = torch.empty(B.moe_route_workspace_size(T, k, E), dtype=torch.uint8, device="cuda")
+    B.moe_route(torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), E, off, counts, offs, poff, st, sw, ps, ws)
+    torch.cuda.synchronize()
+    return {k_: v.cpu().numpy() for k_, v in dict(counts=counts, offsets=offs, padded_offsets=poff,
+                                                   slot_token=st, slot_weight=sw, pair_slot=ps).items()}
+
+
+def _check_route(ids, w, E, off):
+    got = _route_dev(ids, w, E, off)
+    ref = oroute(ids, w, E, off)
+    for k_ in ref:
+        assert np.array_equal(got[k_], ref[k_]), k_
+    return got
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "skew_top1", "skew_top8", "sweep_1k",
+                                  "sweep_64k"])
+def test_route_bit_exact_on_workloads(name):
+    wl = workloads.WORKLOADS[name]
+    ids, w = workloads.routing(wl)
+    _check_route(ids, w, wl.E, wl.expert_offset)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_route_bit_exact_random_with_invalid_ids(seed):
+    r = np.random.default_rng(100 + seed)
+    T, k, E = int(r.integers(1, 3000)), int(r.integers(1, 9)), int(r.integers(1, 257))
+    off = int(r.integers(0, 4)) * E
+    ids = r.integers(-3, 5 * E, (T, k)).astype(np.int32)
+    w = r.random((T, k)).astype(np.float32)
+    _check_route(ids, w, E, off)
+
+
+def test_route_identity_for_sorted_top1():
+    wl = workloads.WORKLOADS["skew_top1"]
+    ids, w = workloads.routing(wl)
+    got = _check_route(ids, w, wl.E, wl.expert_offset)
+    st = got["slot_token"]
+    assert np.array_equal(st[st >= 0], np.arange(wl.T))
+
+
+def test_route_no_local_experts():
+    ids = np.full((40, 3), 999, np.int32)
+    w = np.ones((40, 3), np.float32)
+    got = _check_route(ids, w, 8, 0)
+    assert got["offsets"][-1] == 0 and np.all(got["pair_slot"] == -1)
+
+
+def test_stage_to_slots_bit_exact():
+    wl = workloads.small("slots", T=300, K=512, I=64, E=5, topk=3)
+    ids, w = workloads.routing(wl)
+    x = workloads.activations(wl)
+    rt = oroute(ids, w, wl.E, 0)
+    cap = B.moe_slot_capacity(wl.T, wl.topk, wl.E)
+    a = torch.zeros(cap, wl.K // 2, dtype=torch.uint8, device="cuda")
+    asf = torch.zeros(cap * wl.K // 16, dtype=torch.uint8, device="cuda")
+    gs = torch.zeros(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.moe_stage_workspace_size(), dtype=torch.uint8, device="cuda")
+    B.moe_stage_activation_to_slots(x.cuda(), torch.from_numpy(rt["pair_slot"]).cuda(), wl.topk, cap, a, asf, gs,
+                                    ws=ws)
+    torch.cuda.synchronize()
+    rc, rs, rg = q.quantize(x.float().numpy())
+    valid = rt["slot_token"] >= 0
+    assert np.float32(gs.item()) == rg
+    assert np.array_equal(a.cpu().numpy()[valid], rc[rt["slot_token"][valid]])
+    got_sf = q.unswizzle(asf.cpu().numpy(), cap, wl.K // 16)
+    assert np.array_equal(got_sf[valid], rs[rt["slot_token"][valid]])
+
+
+def test_prepare_weights_layout():
+    r = np.random.default_rng(3)
+    E, I, K = 3, 192, 256
+    sf1 = r.integers(0, 127, (E, 2 * I, K // 16)).astype(np.uint8)
+    sf2 = r.integers(0, 127, (E, K, I // 16)).astype(np.uint8)
+    d1 = torch.empty(sf1.size, dtype=torch.uint8, device="cuda")
+    d2 = torch.empty(sf2.size, dtype=torch.uint8, device="cuda")
+    B.moe_prepare_weights(torch.from_numpy(sf1).cuda(), d1, E, 2 * I, K, B.MOE_PREP_W1)
+    B.moe_prepare_weights(torch.from_numpy(sf2).cuda(), d2, E, K, I, B.MOE_PREP_W2)
+    torch.cuda.synchronize()
+    g1 = d1.cpu().numpy().reshape(E, -1)
+    g2 = d2.cpu().numpy().reshape(E, -1)
+    for e in range(E):
+        assert np.array_equal(q.unswizzle(g2[e], K, I // 16), sf2[e])
+        # W1: atoms hold 64 gate rows then the 64 matching up rows
+        inter = np.concatenate([np.concatenate([sf1[e, 64 * j:64 * j + 64], sf1[e, I + 64 * j:I + 64 * j + 64]])
+                                for j in range(I // 64)])
+        assert np.array_equal(q.unswizzle(g1[e], 2 * I, K // 16), inter)

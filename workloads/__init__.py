@@ -203,5 +203,8 @@ def expert_w2(wl: Workload, e):
 
 def fixed_gs_h(wl: Workload):
     """A fixed (calibrated-mode) global scale for the requantised activation,
-    used where a test needs the h scale without computing every slot."""
-    return np.float32(0.25 / 2688.0)
+    used where a test needs the h scale without computing every slot: the
+    amax of h = silu(g) * u expected at five standard deviations of g and u
+    (std of g ~ 0.02 * sqrt(K) for N(0,1) activations), divided by 2688."""
+    s = 5.0 * 0.02 * np.sqrt(wl.K)
+    return np.float32(max(s * s, 1.0) / 2688.0)
