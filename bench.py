@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 routed-expert MoE layer on one GB300.
+
+A step is one call of the whole layer (moe_forward: routing, global amax,
+quantisation into slots, L1 grouped GEMM with the fused SiLU*up + requant
+epilogue, L2 grouped GEMM with the fused weighted scatter, output cast) over
+one batch of the decode-size workload: T=256 tokens, hidden 4096,
+intermediate 3072, 48 local experts of 384 (rank 3), top-8 uniform routing,
+BF16 N(0,1) activations and NVFP4 weights quantised from N(0, 0.02) (seeded
+synthetic data; no checkpoint).  The h global scale is calibrated once in the
+warm-up (the data-derived scale of a first call) and then held fixed, the
+inference mode of the vllm/nvfp4_cutedsl.py commit pages; x's global scale is
+recomputed every step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (weak scaling: the layer does not shard across GPUs here).
+"""
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="run warm-up + steps of the fixed-gs layer and exit (for ncu); prints nothing")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in getattr(self, "lines", []):
+            f = [v.strip() for v in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [r[0] for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- our arm
+
+def build_layer(wl, R):
+    """BF16 expert weights from the seeded generator, quantised and laid out
+    on the GPU by the library itself."""
+    with cf.ThreadPoolExecutor(8) as ex:
+        w1 = list(ex.map(lambda e: workloads.expert_w1(wl, e), range(wl.E)))
+        w2 = list(ex.map(lambda e: workloads.expert_w2(wl, e), range(wl.E)))
+    layer = R.quantize_weights_on_device(wl, lambda e: w1[e], lambda e: w2[e])
+    del w1, w2
+    return layer
+
+
+def algorithmic(wl, counts):
+    """Bytes and flops the layer must move / do for this routing (real slots only)."""
+    K, I = wl.K, wl.I
+    S = int(counts.sum())
+    touched = int((counts > 0).sum())
+    w1 = touched * 2 * I * (K // 2 + K // 16)
+    w2 = touched * K * (I // 2 + I // 16)
+    a = S * (K // 2 + K // 16)
+    h = S * (I // 2 + I // 16)
+    l1_bytes = w1 + a + h
+    l2_bytes = w2 + h + S * K * 4          # fp32 scatter into the output rows
+    flops_l1 = 2 * S * K * 2 * I
+    flops_l2 = 2 * S * I * K
+    return {"S": S, "touched": touched, "l1_bytes": l1_bytes, "l2_bytes": l2_bytes,
+            "flops_l1": flops_l1, "flops_l2": flops_l2}
+
+
+STAGES = ["route", "stage_x", "gemm_l1", "requant", "gemm_l2", "cast"]
+KERNELS_PER_STEP = {"fixed": 8, "dynamic": 9}  # count, scan, place, amax, quantize, l1, [requant], l2, cast
+
+
+def timed_steps(fw, x, ids, w, steps, warmup, flush, ws):
+    for _ in range(warmup):
+        fw(x, ids, w)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()                       # write 2x L2 between steps: every step starts cold
+        fw(x, ids, w, events=evs[i])
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - t0
+    step_ms = np.array([r[0].elapsed_time(r[6]) for r in evs])
+    stage_ms = {n: float(np.mean([r[j].elapsed_time(r[j + 1]) for r in evs])) for j, n in enumerate(STAGES)}
+    return step_ms, stage_ms, wall
+
+
+def e2e_steps(fw, x_h, ids_h, w_h, x, ids, w, out_h, steps, warmup, ws):
+    """Host buffers in, host result out: H2D of the step's inputs and D2H of the
+    output inside the timed region."""
+    def one():
+        x.copy_(x_h, non_blocking=True)
+        ids.copy_(ids_h, non_blocking=True)
+        w.copy_(w_h, non_blocking=True)
+        out = fw(x, ids, w)
+        out_h.copy_(out, non_blocking=True)
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    return a.elapsed_time(b) / steps
+
+
+def cpu_baseline_oracle(wl, x, ids, w, n_tokens):
+    """The CPU oracle on a bounded sample of the same workload: the layer for
+    the first n_tokens tokens (their own batch), weights of the experts they
+    touch quantised by the oracle beforehand (not timed)."""
+    from oracle import moe as omoe, nvfp4 as oq
+    xs, ids_s, w_s = x[:n_tokens].float().numpy(), ids[:n_tokens], w[:n_tokens]
+    local = ids_s.reshape(-1).astype(np.int64) - wl.expert_offset
+    touched = sorted(set(int(l) for l in local if 0 <= l < wl.E))
+    E, I, K = wl.E, wl.I, wl.K
+    W = {"w1_codes": np.zeros((E, 2 * I, K // 2), np.uint8), "w1_sf": np.zeros((E, 2 * I, K // 16), np.uint8),
+         "gs_w1_gate": np.ones(E, np.float32), "gs_w1_up": np.ones(E, np.float32),
+         "w2_codes": np.zeros((E, K, I // 2), np.uint8), "w2_sf": np.zeros((E, K, I // 16), np.uint8),
+         "gs_w2": np.ones(E, np.float32)}
+    for e in touched:
+        w1 = workloads.expert_w1(wl, e).float().numpy()
+        w2 = workloads.expert_w2(wl, e).float().numpy()
+        W["w1_codes"][e, :I], W["w1_sf"][e, :I], W["gs_w1_gate"][e] = oq.quantize(w1[:I])
+        W["w1_codes"][e, I:], W["w1_sf"][e, I:], W["gs_w1_up"][e] = oq.quantize(w1[I:])
+        W["w2_codes"][e], W["w2_sf"][e], W["gs_w2"][e] = oq.quantize(w2)
+    t0 = time.perf_counter()
+    omoe.forward(xs, ids_s, w_s, E, wl.expert_offset, W)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt, len(touched)
+
+
+def run_ours(args, ws, rank, local):
+    from nvfp4_mixture_experts_stage_gb300 import build
+    build.build()
+    from nvfp4_mixture_experts_stage_gb300 import binding as B, runtime as R
+
+    wl = workloads.WORKLOADS[args.workload]
+    torch.manual_seed(0)
+    x_c = workloads.activations(wl)
+    ids_np, w_np = workloads.routing(wl)
+    layer = build_layer(wl, R)
+    x = x_c.cuda()
+    ids = torch.from_numpy(ids_np).cuda()
+    w = torch.from_numpy(w_np).cuda()
+
+    if args.profile_only:
+        # launches: per step one of each kernel of the fixed-gs layer (L1, L2 alternate)
+        fw = R.Forward(layer, wl.T, B.MOE_GS_FIXED)
+        fw.gs_h.fill_(float(workloads.fixed_gs_h(wl)))
+        for _ in range(args.warmup + args.steps):
+            fw(x, ids, w)
+        torch.cuda.synchronize()
+        if int(fw.status.item()) != 0:
+            raise RuntimeError("device status %d" % int(fw.status.item()))
+        return None
+
+    # warm-up calibration of the h global scale (data-derived), then fixed
+    cal = R.Forward(layer, wl.T, B.MOE_GS_DYNAMIC)
+    cal(x, ids, w)
+    torch.cuda.synchronize()
+    gs_h_cal = float(cal.gs_h.item())
+    fw = R.Forward(layer, wl.T, B.MOE_GS_FIXED)
+    fw.gs_h.fill_(gs_h_cal)
+
+    # bookkeeping for the algorithmic byte count (not part of the timed path)
+    loc = ids_np.reshape(-1).astype(np.int64) - wl.expert_offset
+    counts = np.bincount(loc[(loc >= 0) & (loc < wl.E)], minlength=wl.E)
+    alg = algorithmic(wl, counts)
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    with ClockSampler(local) as clk:
+        step_ms, stage_ms, wall = timed_steps(fw, x, ids, w, args.steps, args.warmup, flush, ws)
+    clocks = clk.summary()
+    st = int(fw.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {B.moe_status_string(st)}")
+
+    # the data-derived (dynamic) h scale mode, same timing discipline
+    dyn_ms, dyn_stage, _ = timed_steps(cal, x, ids, w, max(3, args.steps // 2), 2, flush, ws)
+
+    # end to end through the C ABI with host buffers
+    x_h = x_c.pin_memory()
+    ids_h = torch.from_numpy(ids_np).pin_memory()
+    w_h = torch.from_numpy(w_np).pin_memory()
+    out_h = torch.empty(wl.T, wl.K, dtype=torch.bfloat16).pin_memory()
+    e2e_ms = e2e_steps(fw, x_h, ids_h, w_h, x, ids, w, out_h, args.steps, args.warmup, ws)
+
+    ms = max_over_ranks(float(step_ms.mean()), ws)
+    e2e_ms = max_over_ranks(e2e_ms, ws)
+    pk = peaks()
+    fp4_peak = pk["bf16_tflops"] * 6.0          # dense fp4 / bf16 = 13.5 / 2.25 (nominal ratio)
+    # dominant kernel of the step
+    dom = max(("gemm_l1", "gemm_l2"), key=lambda k: stage_ms[k])
+    dom_ms = stage_ms[dom]
+    dom_bytes = alg["l1_bytes"] if dom == "gemm_l1" else alg["l2_bytes"]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    gemm_ms = stage_ms["gemm_l1"] + stage_ms["gemm_l2"]
+    gemm_tflops = (alg["flops_l1"] + alg["flops_l2"]) / (gemm_ms * 1e-3) / 1e12
+
+    result = {
+        "metric": METRIC,
+        "value": wl.T * ws / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e2m1 -> fp32 accumulate), bf16 activations",
+        "data": "synthetic (seeded numpy PCG64; N(0,1) activations, N(0,0.02) weights quantised on the GPU)",
+        "config": {"workload": f"{wl.name}: T={wl.T}, K={wl.K}, I={wl.I}, E={wl.E} local of 384 (offset "
+                               f"{wl.expert_offset}), top-{wl.topk} uniform",
+                   "tokens_per_step": wl.T, "local_slots": alg["S"], "experts_touched": alg["touched"],
+                   "gs_h": "fixed (calibrated in warm-up)", "gs_x": "dynamic (amax every step)",
+                   "l2": "flushed (256 MB write) between timed steps; weights 1.02 GB > L2",
+                   "parallelism": f"replicas x{ws}"},
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "gemm_tflops": gemm_tflops,
+        "gemm_frac_of_fp4_peak": gemm_tflops / fp4_peak,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes": dom_bytes, "peak_source": pk["source"]},
+        "dynamic_gs_h": {"ms_per_step": float(dyn_ms.mean()), "value": wl.T / (float(dyn_ms.mean()) * 1e-3),
+                         "stage_ms": {k: round(v, 4) for k, v in dyn_stage.items()}},
+        "e2e": {"value": wl.T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4,
+                "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": e2e_ms},
+        "gpu_launches": KERNELS_PER_STEP["fixed"] * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        n = 12
+        v, dt, ne = cpu_baseline_oracle(wl, x_c, ids_np, w_np, n)
+        result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                  "sample": f"first {n} tokens of the {wl.name} batch as their own batch "
+                                            f"({ne} experts touched), oracle forward, {dt:.1f} s"}
+    return result
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args, ws, rank):
+    """The CPU oracle, as it stands, timed on the host cores: each step is the
+    layer for a fixed bounded sample of the workload's tokens."""
+    if rank != 0:
+        return None
+    from oracle import moe as omoe, nvfp4 as oq
+    wl = workloads.WORKLOADS[args.workload]
+    x = workloads.activations(wl)
+    ids, w = workloads.routing(wl)
+    n = 2
+    xs, ids_s, w_s = x[:n].float().numpy(), ids[:n], w[:n]
+    E, I, K = wl.E, wl.I, wl.K
+    W = {"w1_codes": np.zeros((E, 2 * I, K // 2), np.uint8), "w1_sf": np.zeros((E, 2 * I, K // 16), np.uint8),
+         "gs_w1_gate": np.ones(E, np.float32), "gs_w1_up": np.ones(E, np.float32),
+         "w2_codes": np.zeros((E, K, I // 2), np.uint8), "w2_sf": np.zeros((E, K, I // 16), np.uint8),
+         "gs_w2": np.ones(E, np.float32)}
+    touched = sorted(set(int(i) - wl.expert_offset for i in ids_s.reshape(-1)
+                         if 0 <= int(i) - wl.expert_offset < E))
+    for e in touched:
+        w1 = workloads.expert_w1(wl, e).float().numpy()
+        w2 = workloads.expert_w2(wl, e).float().numpy()
+        W["w1_codes"][e, :I], W["w1_sf"][e, :I], W["gs_w1_gate"][e] = oq.quantize(w1[:I])
+        W["w1_codes"][e, I:], W["w1_sf"][e, I:], W["gs_w1_up"][e] = oq.quantize(w1[I:])
+        W["w2_codes"][e], W["w2_sf"][e], W["gs_w2"][e] = oq.quantize(w2)
+    for _ in range(args.warmup):
+        omoe.forward(xs, ids_s, w_s, E, wl.expert_offset, W)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        omoe.forward(xs, ids_s, w_s, E, wl.expert_offset, W)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = n / dt
+    sample = f"first {n} tokens of the {wl.name} batch ({len(touched)} experts touched) per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64 (CPU oracle)", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: T={wl.T}, K={wl.K}, I={wl.I}, E={wl.E}, top-{wl.topk}",
+                   "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        res = run_ours(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

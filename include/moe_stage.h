@@ -260,6 +260,23 @@ moe_status moe_forward(const void* x, int64_t T, int K, int I, int E,
                        void* out, int32_t* dev_status,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_forward with stage timestamps, for tracing and roofline measurement.
+ * stage_events: NULL, or MOE_TRACE_EVENTS cudaEvent_t handles (created by the
+ * caller, with timing enabled) recorded on `stream` at: [0] start, [1] after
+ * routing, [2] after quantising x into the slots, [3] after the L1 GEMM,
+ * [4] after requantising h (equal to [3] in MOE_GS_FIXED mode), [5] after the
+ * L2 GEMM, [6] after the output cast.  While the stream is being captured into
+ * a CUDA graph the records become event-record nodes of the graph.  All other
+ * arguments and behaviour are those of moe_forward. */
+#define MOE_TRACE_EVENTS 7
+moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E,
+                              const int32_t* topk_ids, const float* topk_w, int topk,
+                              int expert_offset, const moe_weights* w,
+                              const float* gs_x_fixed, int gs_h_mode, float* gs_h,
+                              void* out, int32_t* dev_status,
+                              void* ws, size_t ws_bytes, void* const* stage_events,
+                              moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,8 +36,10 @@ EXPORTS = (
     "moe_stage_workspace_size", "moe_workspace_size", "moe_prepare_weights",
     "moe_stage_activation", "moe_stage_activation_to_slots", "moe_route",
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
-    "moe_cast_output", "moe_forward",
+    "moe_cast_output", "moe_forward", "moe_forward_traced",
 )
+
+MOE_TRACE_EVENTS = 7
 
 
 class MoeError(RuntimeError):
@@ -74,6 +76,8 @@ def _load():
         "moe_cast_output": (I32, [P, P, I64, I32, P]),
         "moe_forward": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32, P, P,
                               P, P, SZ, P]),
+        "moe_forward_traced": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32,
+                                     P, P, P, P, SZ, ctypes.POINTER(ctypes.c_void_p), P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -204,3 +208,16 @@ def moe_forward(x, topk_ids, topk_w, E, I, expert_offset, weights, gs_h_mode, gs
         _p(x), T, K, I, E, _p(topk_ids), _p(topk_w), topk, expert_offset, ctypes.byref(weights),
         _p(gs_x_fixed), gs_h_mode, _p(gs_h), _p(out), _p(dev_status), _p(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def moe_forward_traced(x, topk_ids, topk_w, E, I, expert_offset, weights, gs_h_mode, gs_h, out, ws, events,
+                       gs_x_fixed=None, dev_status=None, stream=None):
+    """moe_forward that records MOE_TRACE_EVENTS torch.cuda.Event objects (timing
+    enabled, already created by one record()) at the stage boundaries."""
+    T, K = x.shape
+    topk = topk_ids.shape[1]
+    arr = (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[ev.cuda_event for ev in events])
+    _check("moe_forward_traced", _lib.moe_forward_traced(
+        _p(x), T, K, I, E, _p(topk_ids), _p(topk_w), topk, expert_offset, ctypes.byref(weights),
+        _p(gs_x_fixed), gs_h_mode, _p(gs_h), _p(out), _p(dev_status), _p(ws), ws.numel() * ws.element_size(),
+        arr, _stream(stream)))

@@ -85,6 +85,17 @@ moe_status route_impl(const int32_t* ids, const float* w, int64_t T, int topk, i
              : MOE_ERR_CUDA;
 }
 
+// Record stage event i (if any); inside a graph capture it becomes a record node.
+moe_status mark(void* const* events, int i, cudaStream_t st) {
+  if (!events || !events[i]) return MOE_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = cs == cudaStreamCaptureStatusActive
+                      ? cudaEventRecordWithFlags((cudaEvent_t)events[i], st, cudaEventRecordExternal)
+                      : cudaEventRecord((cudaEvent_t)events[i], st);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 bool shape_ok(int K, int I, int E) {
   return K > 0 && I > 0 && K % 128 == 0 && I % 64 == 0 && E >= 1 && E <= 256;
 }
@@ -285,6 +296,14 @@ moe_status moe_forward(const void* x, int64_t T, int K, int I, int E, const int3
                        int topk, int expert_offset, const moe_weights* w, const float* gs_x_fixed, int gs_h_mode,
                        float* gs_h, void* out, int32_t* dev_status, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
+  return moe_forward_traced(x, T, K, I, E, topk_ids, topk_w, topk, expert_offset, w, gs_x_fixed, gs_h_mode, gs_h,
+                            out, dev_status, ws, ws_bytes, nullptr, stream);
+}
+
+moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, const int32_t* topk_ids,
+                              const float* topk_w, int topk, int expert_offset, const moe_weights* w,
+                              const float* gs_x_fixed, int gs_h_mode, float* gs_h, void* out, int32_t* dev_status,
+                              void* ws, size_t ws_bytes, void* const* stage_events, moe_stream_t stream) {
   if (T < 0 || !w || !gs_h || !ws) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(K, I, E) || topk < 1 || topk > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T > 0 && (!x || !topk_ids || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
@@ -320,32 +339,36 @@ moe_status moe_forward(const void* x, int64_t T, int K, int I, int E, const int3
   float* out32 = reinterpret_cast<float*>(parts[13]);
 
   moe_status s;
+  if (mark(stage_events, 0, stream) != MOE_OK) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
   s = route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, poff, slot_token, slot_weight,
                  pair_slot, cap, rcnt, rbase, dev_status, stream);
-  if (s != MOE_OK) return s;
+  if (s != MOE_OK || (s = mark(stage_events, 1, stream)) != MOE_OK) return s;
   if (!gs_x_fixed) {
     s = amax_launch(x, T, K, K, x_amax, stream);
     if (s != MOE_OK) return s;
   }
   s = quantize_launch(2, x, T, K, K, gs_x_fixed ? nullptr : x_amax, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk,
                       nullptr, cap, dev_status, stream);
-  if (s != MOE_OK) return s;
+  if (s != MOE_OK || (s = mark(stage_events, 2, stream)) != MOE_OK) return s;
   if (gs_h_mode == MOE_GS_DYNAMIC) {
     s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
                        w->gs_w1_up, MOE_L1_SILU_BF16, h_bf16, h_amax, nullptr, nullptr, nullptr, dev_status, stream);
-    if (s != MOE_OK) return s;
+    if (s != MOE_OK || (s = mark(stage_events, 3, stream)) != MOE_OK) return s;
     s = quantize_launch(3, h_bf16, cap, I, I, reinterpret_cast<const uint32_t*>(h_amax), nullptr, gs_h, h_fp4, h_sf,
                         nullptr, 0, slot_token, cap, dev_status, stream);
   } else {
     s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
                        w->gs_w1_up, MOE_L1_SILU_REQUANT, nullptr, nullptr, h_fp4, h_sf, gs_h, dev_status, stream);
+    if (s != MOE_OK || (s = mark(stage_events, 3, stream)) != MOE_OK) return s;
   }
-  if (s != MOE_OK) return s;
+  if (s != MOE_OK || (s = mark(stage_events, 4, stream)) != MOE_OK) return s;
   s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2, MOE_L2_SCATTER,
                      nullptr, slot_token, slot_weight, out32, T, dev_status, stream);
+  if (s != MOE_OK || (s = mark(stage_events, 5, stream)) != MOE_OK) return s;
+  s = moe_cast_output(out32, out, T, K, stream);
   if (s != MOE_OK) return s;
-  return moe_cast_output(out32, out, T, K, stream);
+  return mark(stage_events, 6, stream);
 }
 
 }  // extern "C"

@@ -109,11 +109,16 @@ class Forward:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.wstruct = layer.weights_struct()
 
-    def __call__(self, x, topk_ids, topk_w, gs_x_fixed=None, stream=None):
+    def __call__(self, x, topk_ids, topk_w, gs_x_fixed=None, stream=None, events=None):
         L = self.layer
-        B.moe_forward(x, topk_ids, topk_w, L.E, L.I, L.expert_offset, self.wstruct, self.gs_h_mode,
-                      self.gs_h, self.out, self.ws, gs_x_fixed=gs_x_fixed, dev_status=self.status,
-                      stream=stream)
+        if events is None:
+            B.moe_forward(x, topk_ids, topk_w, L.E, L.I, L.expert_offset, self.wstruct, self.gs_h_mode,
+                          self.gs_h, self.out, self.ws, gs_x_fixed=gs_x_fixed, dev_status=self.status,
+                          stream=stream)
+        else:
+            B.moe_forward_traced(x, topk_ids, topk_w, L.E, L.I, L.expert_offset, self.wstruct, self.gs_h_mode,
+                                 self.gs_h, self.out, self.ws, events, gs_x_fixed=gs_x_fixed,
+                                 dev_status=self.status, stream=stream)
         return self.out
 
 
