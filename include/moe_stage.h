@@ -177,6 +177,32 @@ moe_status moe_route(const int32_t* topk_ids, const float* topk_w, int64_t T, in
                      int32_t* slot_token, float* slot_weight, int32_t* pair_slot,
                      int64_t capacity, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route for callers that cannot allocate (the commit pages have no
+ * counterpart: this is an addition of this library).  Some callers have no
+ * allocator at hand when they route: a plugin whose host runtime owns all
+ * device memory and passes in only the call's tensors, or a serving loop that
+ * must never allocate on its hot path.  This entry point takes the same
+ * arguments as moe_route minus ws/ws_bytes, writes the same outputs (bit for
+ * bit), and allocates nothing: its two scratch tables live in a fixed array in
+ * the library's own device memory, 2 * MOE_ROUTE_STATIC_TABLE_INTS int32
+ * (2 MiB), held by every GPU that loads the library until the process exits.
+ *   Limit: ceil(T*topk/256) * E <= MOE_ROUTE_STATIC_TABLE_INTS (for E = 48 about
+ *   1.39 million (token, k) pairs); larger calls return MOE_ERR_UNSUPPORTED_SHAPE
+ *   without enqueuing anything.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before capturing a
+ *   stream.
+ *   Every call shares the one array.  Calls ordered on one stream are safe; calls
+ *   that can overlap on the GPU (other streams, other host threads) race on it and
+ *   corrupt each other's routing.  Nothing needs clearing between calls: both
+ *   tables are rewritten in full before they are read. */
+#define MOE_ROUTE_STATIC_TABLE_INTS 262144
+moe_status moe_route_static_scratch(const int32_t* topk_ids, const float* topk_w, int64_t T, int topk,
+                                    int E, int expert_offset,
+                                    int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                                    int32_t* slot_token, float* slot_weight, int32_t* pair_slot,
+                                    int64_t capacity, moe_stream_t stream);
+
 /* L1 grouped GEMM, gate|up (nvfp4_mega_moe_l1 of the nvfp4_mega_moe.py commits;
  * split at I per the vllm/nvfp4_cutedsl.py "intermediate_size" commit).
  * For every expert e and slot row p in [padded_offsets[e], padded_offsets[e] +

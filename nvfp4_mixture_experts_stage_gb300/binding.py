@@ -36,8 +36,10 @@ EXPORTS = (
     "moe_stage_workspace_size", "moe_workspace_size", "moe_prepare_weights",
     "moe_stage_activation", "moe_stage_activation_to_slots", "moe_route",
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
-    "moe_cast_output", "moe_forward", "moe_forward_traced",
+    "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
 )
+
+MOE_ROUTE_STATIC_TABLE_INTS = 262144
 
 MOE_TRACE_EVENTS = 7
 
@@ -70,6 +72,7 @@ def _load():
         "moe_stage_activation": (I32, [P, I64, I32, I64, P, P, I32, P, P, P, SZ, P, P]),
         "moe_stage_activation_to_slots": (I32, [P, I64, I32, I64, P, I32, I64, P, P, P, P, P, SZ, P, P]),
         "moe_route": (I32, [P, P, I64, I32, I32, I32, P, P, P, P, P, P, I64, P, SZ, P]),
+        "moe_route_static_scratch": (I32, [P, P, I64, I32, I32, I32, P, P, P, P, P, P, I64, P]),
         "moe_grouped_gemm_l1": (I32, [P, P, P, P, P, I32, I64, I32, I32, P, P, P, P, I32, P, P, P, P, P, P, P]),
         "moe_requant": (I32, [P, I64, I32, P, P, P, P, P, P, P]),
         "moe_grouped_gemm_l2": (I32, [P, P, P, P, P, I32, I64, I32, I32, P, P, P, I32, P, P, P, P, I64, P, P]),
@@ -161,6 +164,16 @@ def moe_route(topk_ids, topk_w, E, expert_offset, counts, offsets, padded_offset
         _p(topk_ids), _p(topk_w), T, topk, E, expert_offset, _p(counts), _p(offsets), _p(padded_offsets),
         _p(slot_token), _p(slot_weight), _p(pair_slot), slot_token.numel(), _p(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_route_static_scratch(topk_ids, topk_w, E, expert_offset, counts, offsets, padded_offsets, slot_token,
+                             slot_weight, pair_slot, stream=None):
+    """moe_route without a workspace (its scratch is a fixed device array inside
+    the library; see include/moe_stage.h for the size limit and the rules)."""
+    T, topk = topk_ids.shape
+    _check("moe_route_static_scratch", _lib.moe_route_static_scratch(
+        _p(topk_ids), _p(topk_w), T, topk, E, expert_offset, _p(counts), _p(offsets), _p(padded_offsets),
+        _p(slot_token), _p(slot_weight), _p(pair_slot), slot_token.numel(), _stream(stream)))
 
 
 def moe_grouped_gemm_l1(a_fp4, a_sf, gs_a, offsets, padded_offsets, E, K, I, w1_fp4, w1_sf, gs_w1_gate,
