@@ -255,6 +255,27 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const 
                                float* out32, int64_t T,
                                int32_t* dev_status, moe_stream_t stream);
 
+/* Which grouped-GEMM kernel moe_grouped_gemm_l1/l2 and moe_forward launch
+ * (process-wide setting; returns the previous one; not synchronised with work in
+ * flight, so set it between calls):
+ *   MOE_GEMM_AUTO      (default) the weight-streaming kernel when the slot capacity
+ *                      implies at most 64 slots per local expert on average
+ *                      (capacity - 127*E <= 64*E) and the contraction is <= 4096,
+ *                      the tiled kernel otherwise;
+ *   MOE_GEMM_TILED     always the tiled kernel: 128 slot rows x 128 weight rows per
+ *                      tile, slots on the MMA's M side;
+ *   MOE_GEMM_STREAMING the weight-streaming kernel whenever the contraction is
+ *                      <= 4096: weight rows on the MMA's M side, chunks of up to 64
+ *                      slots on its N side, the chunk's activation scales resident
+ *                      in tensor memory.  Experts with more than 64 slots are split
+ *                      into several chunks, each streaming the expert's weights.
+ * Both kernels compute the same arithmetic (results may differ in the fp32
+ * summation order only). */
+#define MOE_GEMM_AUTO      0
+#define MOE_GEMM_TILED     1
+#define MOE_GEMM_STREAMING 2
+int moe_set_gemm_policy(int policy);
+
 /* out_bf16[i] = bf16(out32[i]) for i < T*K (round to nearest even). */
 moe_status moe_cast_output(const float* out32, void* out_bf16, int64_t T, int K,
                            moe_stream_t stream);

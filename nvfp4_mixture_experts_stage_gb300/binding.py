@@ -37,7 +37,10 @@ EXPORTS = (
     "moe_stage_activation", "moe_stage_activation_to_slots", "moe_route",
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
     "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
+    "moe_set_gemm_policy",
 )
+
+MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
 
 MOE_ROUTE_STATIC_TABLE_INTS = 262144
 
@@ -77,6 +80,7 @@ def _load():
         "moe_requant": (I32, [P, I64, I32, P, P, P, P, P, P, P]),
         "moe_grouped_gemm_l2": (I32, [P, P, P, P, P, I32, I64, I32, I32, P, P, P, I32, P, P, P, P, I64, P, P]),
         "moe_cast_output": (I32, [P, P, I64, I32, P]),
+        "moe_set_gemm_policy": (I32, [I32]),
         "moe_forward": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32, P, P,
                               P, P, SZ, P]),
         "moe_forward_traced": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32,
@@ -127,6 +131,15 @@ def moe_stage_workspace_size():
 
 def moe_workspace_size(T_max, K, I, E, topk):
     return _lib.moe_workspace_size(T_max, K, I, E, topk)
+
+
+def moe_set_gemm_policy(policy):
+    """Select the grouped-GEMM kernel (MOE_GEMM_AUTO / _TILED / _STREAMING);
+    returns the previous policy."""
+    r = _lib.moe_set_gemm_policy(policy)
+    if r < 0:
+        raise MoeError("moe_set_gemm_policy", MOE_ERR_INVALID_ARG)
+    return r
 
 
 def moe_status_string(s):

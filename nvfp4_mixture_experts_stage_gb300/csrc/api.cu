@@ -117,6 +117,11 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
+int moe_set_gemm_policy(int policy) {
+  if (policy != MOE_GEMM_AUTO && policy != MOE_GEMM_TILED && policy != MOE_GEMM_STREAMING) return -1;
+  return set_gemm_policy(policy);
+}
+
 int64_t moe_slot_capacity(int64_t T, int topk, int E) {
   if (T < 0 || topk < 1 || E < 1) return -1;
   return ceil_div(T * topk + (int64_t)(kTileM - 1) * E, kTileM) * kTileM;
@@ -242,7 +247,7 @@ moe_status moe_grouped_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const 
       if (!out_bf16 || !aligned(out_bf16, 16)) return MOE_ERR_INVALID_ARG;
       break;
     case MOE_L1_SILU_REQUANT:
-      if (!h_fp4 || !h_sf || !gs_h || !aligned(h_fp4, 8) || !aligned(h_sf, 4)) return MOE_ERR_INVALID_ARG;
+      if (!h_fp4 || !h_sf || !gs_h || !aligned(h_fp4, 16) || !aligned(h_sf, 4)) return MOE_ERR_INVALID_ARG;
       if (out_bf16 && !aligned(out_bf16, 16)) return MOE_ERR_INVALID_ARG;
       break;
     default: return MOE_ERR_INVALID_ARG;

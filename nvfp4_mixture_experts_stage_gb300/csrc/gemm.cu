@@ -23,10 +23,7 @@
 // Tiles are (expert, n-tile, m-tile) with the m-tiles of one weight block adjacent,
 // so CTAs running at the same time share weight tiles through L2; the expert of a
 // tile comes from the padded offsets on the device (no host sync).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "kernels.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 
@@ -87,113 +84,11 @@ struct __align__(1024) GemmSmem {
   int cnt[256];
 };
 
-// ----------------------------------------------------------------------------- PTX
-MOE_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-MOE_DEV void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-MOE_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-MOE_DEV void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-MOE_DEV void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-MOE_DEV void tc_mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
-          "r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-      : "memory");
-}
-// 16 consecutive fp32 columns of this thread's TMEM lane; the wait sits in the same
-// asm statement so no use of the outputs can be scheduled before it.
-MOE_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B, 8-row
-// groups 1024 B apart (SBO), descriptor version 1, swizzle mode 2 (128B).
-MOE_DEV uint64_t sdesc_sw128(const void* p) {
-  const uint64_t addr = smem_u32(p);
-  return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
-         (2ull << 61);
-}
-// Descriptor of one 512-byte scale atom seen as 32 rows x 16 B, no swizzle.
-MOE_DEV uint64_t sdesc_sf(const void* p) {
-  const uint64_t addr = smem_u32(p);
-  return ((addr & 0x3FFFFull) >> 4) | ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
-}
-// Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), K-major, UE4M3
-// scales (scale format 0), scale-factor ids 0, N >> 3 at bit 17, M >> 4 at bit 24.
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 
-// Bounded wait: false on timeout (sets the abort flag and the status word) or when
-// another role already aborted.
+// Bounded wait through the CTA's abort flag.
 MOE_DEV bool wait_bar(uint64_t* bar, uint32_t parity, GemmSmem& s, int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 255u) == 0) {
-      if (*(volatile int*)&s.abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *(volatile int*)&s.abort_flag = 1;
-        set_status(status, MOE_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-  return true;
+  return wait_bar_bounded(bar, parity, &s.abort_flag, status);
 }
 
 // Tile t -> (expert, n-tile, m-tile); e advances monotonically with t.
@@ -209,11 +104,6 @@ struct TileCursor {
     return true;
   }
 };
-
-MOE_DEV float silu_mul(float g, float u) {
-  const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-  return round_bf16(__fmul_rn(s, u));
-}
 
 template <int KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -486,45 +376,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-// ----------------------------------------------------------------------------- host
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// Row-major byte matrix [rows, row_bytes] as a 2-D uint8 tensor map with a
-// 128-byte-swizzled box of box_rows x 128 B.
-static bool make_tmap(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {row_bytes, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)kBKBytes, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-static int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  }
-  return n;
-}
-
 constexpr size_t kGemmSmemBytes = sizeof(GemmSmem) + 1024;
 
 template <int KIND>
@@ -540,12 +391,30 @@ static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, cons
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+static int g_policy = MOE_GEMM_AUTO;
+
+int gemm_policy() { return __atomic_load_n(&g_policy, __ATOMIC_RELAXED); }
+
+int set_gemm_policy(int policy) { return __atomic_exchange_n(&g_policy, policy, __ATOMIC_RELAXED); }
+
+// Small per-expert slot counts (at most 64 slots per local expert on average even if
+// every pair were local): stream the weights with the slot chunk on the MMA's N side.
+bool use_stream_gemm(int64_t cap, int E, int Kred) {
+  const int pol = gemm_policy();
+  if (pol == MOE_GEMM_TILED || !stream_gemm_supported(Kred)) return false;
+  if (pol == MOE_GEMM_STREAMING) return true;
+  return cap - (int64_t)(kTileM - 1) * E <= (int64_t)64 * E;
+}
+
 // L1: A = slot activations [cap, K/2]; B = W1 [E*2I, K/2]; N per tile = 64 h cols.
 moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,
                           const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
                           const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
                           float* h_amax, uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h, int32_t* status,
                           cudaStream_t st) {
+  if (use_stream_gemm(cap, E, K))
+    return launch_stream_gemm_l1(a_fp4, a_sf, gs_a, offsets, padded_offsets, E, cap, K, I, w1_fp4, w1_sf, gs_g, gs_u,
+                                 epilogue, out_bf16, h_amax, h_fp4, h_sf, gs_h, status, st);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w1_fp4, (uint64_t)K / 2, (uint64_t)E * 2 * I, 64)) return MOE_ERR_CUDA;
@@ -586,6 +455,9 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
                           const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
                           const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
                           int32_t* status, cudaStream_t st) {
+  if (use_stream_gemm(cap, E, I))
+    return launch_stream_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, cap, I, K, w2_fp4, w2_sf, gs_w2,
+                                 epilogue, y_rows, slot_token, slot_weight, out32, T, status, st);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, kBN)) return MOE_ERR_CUDA;

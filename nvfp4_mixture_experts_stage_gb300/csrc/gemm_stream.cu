@@ -1,0 +1,527 @@
+// Weight-streaming grouped NVFP4 GEMM for small per-expert slot counts (decode).
+//
+// Same layer arithmetic as the tiled kernel in gemm.cu (nvfp4-megamoe-kernel commits
+// of src/nvfp4_megamoe_kernel/nvfp4_mega_moe.py: D = alpha * A @ B per expert; of
+// vllm/nvfp4_cutedsl.py: gate | up split at I; of tests: SiLU(gate)*up, requantise,
+// weighted scatter), organised for the case where every expert owns only a few
+// slots and the weights must simply stream from HBM:
+//
+//   * operands are swapped: the MMA's M=128 side is a block of weight rows and
+//     its N=64 side is a chunk of up to 64 slot rows of one expert, so D^T sits in
+//     TMEM with one weight row per lane;
+//   * the chunk's activation scales are copied into TMEM once per chunk and stay
+//     there for the whole contraction, so each pipeline stage copies only the four
+//     weight-scale atoms it brings (the tiled kernel copies eight);
+//   * each CTA walks a contiguous range of (expert, chunk, weight-block) tiles, so
+//     consecutive tiles reuse the resident activation scales;
+//   * warp 6 builds the TMEM images of the next chunk's activation scales in shared
+//     memory while the current chunk runs.
+//
+// Scale-factor placement read by kind::mxf4nvf4.block_scale.scale_vec::4X (M=128):
+// operand A row m at TMEM lane m, column base + m/32; operand B row n at lane n%32,
+// column base + n/32; bases 4-column aligned.  A 512-byte atom copied with
+// tcgen05.cp.32x128b.warpx4 satisfies the A placement directly; the B images put
+// the chunk's rows i and 32+i in bytes 0..3 and 4..7 of image row i.
+#include "tcgen05.cuh"
+
+namespace moe {
+namespace stream {
+
+constexpr int kChunk = 64;                    // slots per chunk (MMA N)
+constexpr int kStages = 6;
+constexpr int kWStage = 128 * 128;            // 16 KB: 128 weight rows x 256 fp4
+constexpr int kBStage = kChunk * 128;         // 8 KB: 64 slot rows x 256 fp4
+constexpr int kSfwStage = 4 * 512;            // 4 weight-scale atoms
+constexpr int kThreads = 224;                 // 7 warps
+constexpr int kTmemCols = 512;
+constexpr int kMaxKSteps = 64;                // contraction <= 4096
+constexpr int kSfbBase = 2 * kChunk;          // 128: two accumulators of 64 columns first
+constexpr int kSfwBase = kSfbBase + 4 * kMaxKSteps;  // 384; stage s at 384 + 16 s (< 480)
+constexpr int kStageLd = 72;                  // padded row of the L1 exchange buffers (bf16)
+
+constexpr uint32_t kIdesc =
+    (1u << 7) | (1u << 10) | ((uint32_t)(kChunk >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+enum Kind : int { kL1GateUp = 0, kL1Silu = 1, kL1Requant = 2, kL2Rows = 3, kL2Scatter = 4 };
+
+struct Params {
+  const uint8_t* a_sf;              // slot-row scales, 512-byte atoms [cap/128][Kred/64]
+  const uint8_t* w_sf;              // prepared weight scales [E][w_rows/128][Kred/64]
+  const int32_t* offsets;
+  const int32_t* padded_offsets;
+  int E;
+  int Kred;
+  int n_tiles;                      // weight blocks per expert
+  int w_rows;                       // weight rows per expert
+  int I;
+  const float* gs_a;
+  const float* gs_w0;               // L1 gate / L2 down
+  const float* gs_w1;               // L1 up
+  void* out_bf16;
+  int64_t out_ld;
+  float* h_amax;
+  uint8_t* h_fp4;
+  uint8_t* h_sf;
+  const float* gs_h;
+  const int32_t* slot_token;
+  const float* slot_weight;
+  float* out32;
+  int64_t T;
+  int out_cols;
+  int64_t cap;
+  int32_t* status;
+};
+
+struct __align__(1024) Smem {
+  uint8_t w[kStages][kWStage];
+  uint8_t b[kStages][kBStage];
+  uint8_t sfw[kStages][kSfwStage];
+  uint8_t img[kMaxKSteps][512];
+  uint16_t xg[kChunk][kStageLd];    // L1 exchange: gate values [slot][h col] (bf16 bits)
+  uint16_t xu[kChunk][kStageLd];    //              up values
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint64_t fin;
+  uint64_t img_full;
+  uint64_t img_free;
+  uint32_t tmem_base;
+  int abort_flag;
+  int bad_offsets;
+  int poff[257];
+  int cnt[256];
+  int cum[257];                     // tiles before expert e
+};
+
+// Tile t -> (expert, chunk, weight block); e advances monotonically with t.
+struct Cursor {
+  int e = 0;
+  MOE_DEV void locate(const Smem& s, int n_tiles, int t, int& c, int& n) {
+    while (t >= s.cum[e + 1]) ++e;
+    const int local = t - s.cum[e];
+    c = local / n_tiles;
+    n = local - c * n_tiles;
+  }
+};
+
+MOE_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    stream_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                       const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr bool kL1 = KIND <= kL1Requant;
+
+  if (threadIdx.x == 0) s.bad_offsets = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.poff[i] = p.padded_offsets[i];
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s.cnt[i] = p.offsets[i + 1] - p.offsets[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
+    const int lo = s.poff[i], hi = s.poff[i + 1], c = s.cnt[i];
+    if (lo < 0 || hi < lo || (lo & 127) || (hi & 127) || c < 0 || c > hi - lo || hi > p.cap) s.bad_offsets = 1;
+  }
+  if (warp == 0) {
+    // tiles per expert = chunks * weight blocks; exclusive scan over experts
+    int run = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < p.E ? ((max(s.cnt[e], 0) + kChunk - 1) / kChunk) * p.n_tiles : 0;
+      int incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += t;
+      }
+      if (e < p.E) s.cum[e] = run + incl - v;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) s.cum[p.E] = run;
+  }
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 4);
+    }
+    mbar_init(&s.drain, 1);
+    mbar_init(&s.fin, 1);
+    mbar_init(&s.img_full, 1);
+    mbar_init(&s.img_free, 1);
+    s.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  const bool bad = s.bad_offsets != 0;
+  if (bad && threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE_INDEX);
+  const int total = bad ? 0 : s.cum[p.E];
+  const int t_lo = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
+  const int t_hi = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  const int nkb = (p.Kred + 255) >> 8;
+  const int ksf4 = p.Kred >> 6;  // k-steps (scale atoms per 128 rows)
+  int* abort_flag = &s.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[kStages];
+      bool issued[kStages];
+      for (int i = 0; i < kStages; ++i) issued[i] = false;
+      bool ok = true;
+      Cursor cur;
+      for (int t = t_lo; t < t_hi && ok; ++t) {
+        int c, n;
+        cur.locate(s, p.n_tiles, t, c, n);
+        const int e = cur.e;
+        const int row_x = s.poff[e] + c * kChunk;
+        const uint8_t* sfw_src = p.w_sf + ((int64_t)e * (p.w_rows >> 7) + n) * (int64_t)ksf4 * 512;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int natoms = min(4, ksf4 - 4 * kb);
+          if (!wait_bar_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.full[stage], kWStage + kBStage + natoms * 512);
+          const int x = kb * 128;
+          if (kL1) {
+            const int yw = e * p.w_rows + n * 64;
+            tma_load_2d(s.w[stage], &tmap_w, &s.full[stage], x, yw);
+            tma_load_2d(s.w[stage] + kWStage / 2, &tmap_w, &s.full[stage], x, yw + p.I);
+          } else {
+            tma_load_2d(s.w[stage], &tmap_w, &s.full[stage], x, e * p.w_rows + n * 128);
+          }
+          tma_load_2d(s.b[stage], &tmap_x, &s.full[stage], x, row_x);
+          bulk_load(s.sfw[stage], sfw_src + kb * 4 * 512, natoms * 512, &s.full[stage]);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok || *(volatile int*)abort_flag)
+        for (int i = 0; i < kStages; ++i)
+          if (issued[i]) wait_bar_drain(&s.full[i], issued_phase[i]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0, ch = -1, last_e = -1, last_c = -1;
+      Cursor cur;
+      for (int t = t_lo; t < t_hi && ok; ++t, ++it) {
+        int c, n;
+        cur.locate(s, p.n_tiles, t, c, n);
+        if (cur.e != last_e || c != last_c) {
+          // new chunk: let the MMAs reading the old activation scales finish, then
+          // copy the new chunk's scale images into TMEM
+          ++ch;
+          last_e = cur.e;
+          last_c = c;
+          if (ch > 0) {
+            tc_commit(&s.drain);
+            if (!wait_bar_bounded(&s.drain, (ch - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          }
+          if (!wait_bar_bounded(&s.img_full, ch & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          for (int k = 0; k < ksf4; ++k) tc_cp_sf(tmem + kSfbBase + 4 * k, sdesc_sf(s.img[k]));
+          tc_commit(&s.img_free);
+        }
+        const int acc = it & 1;
+        if (!wait_bar_bounded(&s.tempty[acc], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * kChunk;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int natoms = min(4, ksf4 - 4 * kb);
+          if (!wait_bar_bounded(&s.full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sfw_col = tmem + kSfwBase + 16 * stage;
+          for (int a = 0; a < natoms; ++a) tc_cp_sf(sfw_col + 4 * a, sdesc_sf(s.sfw[stage] + 512 * a));
+          for (int kk = 0; kk < natoms; ++kk)
+            tc_mma_fp4(d, sdesc_sw128(s.w[stage] + 32 * kk), sdesc_sw128(s.b[stage] + 32 * kk), kIdesc,
+                       sfw_col + 4 * kk, tmem + kSfbBase + 4 * (4 * kb + kk), (kb | kk) != 0);
+          tc_commit(&s.empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&s.tfull[acc]);
+      }
+      tc_commit(&s.fin);
+      wait_bar_drain(&s.fin, 0);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ activation-scale images
+    int ch = -1, last_e = -1, last_c = -1;
+    Cursor cur;
+    for (int t = t_lo; t < t_hi; ++t) {
+      int c, n;
+      cur.locate(s, p.n_tiles, t, c, n);
+      if (cur.e == last_e && c == last_c) continue;
+      ++ch;
+      last_e = cur.e;
+      last_c = c;
+      if (!wait_bar_bounded(&s.img_free, (ch & 1) ^ 1, abort_flag, p.status)) break;
+      // image row i (16 B): scales of chunk rows i and 32+i for k-step k, then zeros
+      const int64_t r0 = (int64_t)s.poff[cur.e] + c * kChunk + lane;
+      const int64_t r1 = r0 + 32;
+      const uint8_t* base0 = p.a_sf + (r0 >> 7) * (int64_t)ksf4 * 512 + (r0 & 31) * 16 + ((r0 >> 5) & 3) * 4;
+      const uint8_t* base1 = p.a_sf + (r1 >> 7) * (int64_t)ksf4 * 512 + (r1 & 31) * 16 + ((r1 >> 5) & 3) * 4;
+      for (int k = 0; k < ksf4; ++k) {
+        const uint32_t s0 = __ldg(reinterpret_cast<const uint32_t*>(base0 + k * 512));
+        const uint32_t s1 = __ldg(reinterpret_cast<const uint32_t*>(base1 + k * 512));
+        *reinterpret_cast<uint4*>(&s.img[k][lane * 16]) = make_uint4(s0, s1, 0u, 0u);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.img_full);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;           // TMEM lane quarter = weight rows 32q..32q+31
+    const int tid = threadIdx.x - 64; // 0..127 over the four epilogue warps
+    int it = 0;
+    Cursor cur;
+    float amax = 0.0f;
+    for (int t = t_lo; t < t_hi; ++t, ++it) {
+      int c, n;
+      cur.locate(s, p.n_tiles, t, c, n);
+      const int e = cur.e;
+      const int acc = it & 1;
+      wait_bar_bounded(&s.tfull[acc], (it >> 1) & 1, abort_flag, p.status);
+      epi_bar();  // every epilogue warp has arrived (and sees an abort set before)
+      if (*(volatile int*)abort_flag) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kChunk;
+      float v[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; j += 16) tmem_ld16(taddr + j, *reinterpret_cast<float(*)[16]>(&v[j]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty[acc]);  // accumulator free: values are in registers
+
+      const int cnt_c = min(kChunk, s.cnt[e] - c * kChunk);  // valid slots of this chunk
+      const int64_t row0 = (int64_t)s.poff[e] + c * kChunk;
+      if (kL1) {
+        const float gs_a = __ldg(p.gs_a);
+        const bool up = q >= 2;
+        const float alpha = __fmul_rn(gs_a, __ldg((up ? p.gs_w1 : p.gs_w0) + e));
+        const int col = (q & 1) * 32 + lane;  // h column within the 64-column block
+        uint16_t (*x)[kStageLd] = up ? s.xu : s.xg;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j)
+          if (j < cnt_c) x[j][col] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(alpha, v[j])));
+        epi_bar();  // exchange complete
+        const int sl = tid >> 1, hb = tid & 1;  // slot, 32-column half
+        if (sl < cnt_c) {
+          const int64_t prow = row0 + sl;
+          const int hcol = n * 64 + hb * 32;
+          float g[32], u[32];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const uint32_t gw = *reinterpret_cast<const uint32_t*>(&s.xg[sl][hb * 32 + i]);
+            const uint32_t uw = *reinterpret_cast<const uint32_t*>(&s.xu[sl][hb * 32 + i]);
+            g[i] = bf16lo(gw); g[i + 1] = bf16hi(gw);
+            u[i] = bf16lo(uw); u[i + 1] = bf16hi(uw);
+          }
+          if (KIND == kL1GateUp) {
+            uint4* dg = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + hcol);
+            uint4* du = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + p.I + hcol);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              dg[i] = make_uint4(pack_bf16x2(g[8 * i], g[8 * i + 1]), pack_bf16x2(g[8 * i + 2], g[8 * i + 3]),
+                                 pack_bf16x2(g[8 * i + 4], g[8 * i + 5]), pack_bf16x2(g[8 * i + 6], g[8 * i + 7]));
+              du[i] = make_uint4(pack_bf16x2(u[8 * i], u[8 * i + 1]), pack_bf16x2(u[8 * i + 2], u[8 * i + 3]),
+                                 pack_bf16x2(u[8 * i + 4], u[8 * i + 5]), pack_bf16x2(u[8 * i + 6], u[8 * i + 7]));
+            }
+          } else {
+            float h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = silu_mul(g[i], u[i]);
+            if (KIND == kL1Silu) {
+              uint4* dh = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + hcol);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dh[i] = make_uint4(pack_bf16x2(h[8 * i], h[8 * i + 1]), pack_bf16x2(h[8 * i + 2], h[8 * i + 3]),
+                                   pack_bf16x2(h[8 * i + 4], h[8 * i + 5]), pack_bf16x2(h[8 * i + 6], h[8 * i + 7]));
+#pragma unroll
+              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+            } else {
+              const float rg = recip_global_scale(__ldg(p.gs_h));
+              uint32_t sfw = 0, cw[4];
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {  // two 16-element blocks
+                float bm = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(h[16 * b + i]));
+                float rb;
+                sfw |= block_scale(bm, rg, rb) << (8 * b);
+#pragma unroll
+                for (int w4 = 0; w4 < 2; ++w4) {
+                  uint32_t word = 0;
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const float lo = h[16 * b + 8 * w4 + 2 * i], hi = h[16 * b + 8 * w4 + 2 * i + 1];
+                    const uint32_t byte =
+                        e2m1x2(code_mag(fabsf(lo), rg, rb), code_mag(fabsf(hi), rg, rb)) | sign_bits2(lo, hi);
+                    word |= byte << (8 * i);
+                  }
+                  cw[2 * b + w4] = word;
+                }
+              }
+              *reinterpret_cast<uint4*>(p.h_fp4 + prow * (p.I >> 1) + (hcol >> 1)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+              *reinterpret_cast<uint16_t*>(p.h_sf + sf_swizzle_offset(prow, hcol >> 4, p.I >> 4)) = (uint16_t)sfw;
+            }
+          }
+        }
+        epi_bar();  // exchange buffers may be overwritten by the next tile
+      } else {
+        const float alpha = __fmul_rn(__ldg(p.gs_a), __ldg(p.gs_w0 + e));
+        const int col = n * 128 + q * 32 + lane;  // output column
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          if (j < cnt_c) {
+            const float y = round_bf16(__fmul_rn(alpha, v[j]));
+            const int64_t prow = row0 + j;
+            if (KIND == kL2Rows) {
+              reinterpret_cast<__nv_bfloat16*>(p.out_bf16)[prow * p.out_ld + col] = __float2bfloat16_rn(y);
+            } else {
+              const int32_t tok = __ldg(p.slot_token + prow);
+              if (tok >= p.T) {
+                set_status(p.status, MOE_ERR_DEVICE_INDEX);
+              } else if (tok >= 0) {
+                atomicAdd(p.out32 + (int64_t)tok * p.out_cols + col, __fmul_rn(__ldg(p.slot_weight + prow), y));
+              }
+            }
+          }
+        }
+      }
+    }
+    if (KIND == kL1Silu && p.h_amax) {
+      const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
+      if (lane == 0 && mb) atomicMax(reinterpret_cast<uint32_t*>(p.h_amax), mb);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+template <int KIND>
+static moe_status launch_kind(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(stream_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured = true;
+  }
+  stream_gemm_kernel<KIND><<<num_sms(), kThreads, kSmemBytes, st>>>(tw, tx, p);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace stream
+
+bool stream_gemm_supported(int Kred) { return Kred <= 64 * stream::kMaxKSteps; }
+
+moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,
+                                 const int32_t* padded_offsets, int E, int64_t cap, int K, int I,
+                                 const uint8_t* w1_fp4, const uint8_t* w1_sf, const float* gs_g, const float* gs_u,
+                                 int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4, uint8_t* h_sf,
+                                 const float* gs_h, int32_t* status, cudaStream_t st) {
+  using namespace stream;
+  CUtensorMap tw, tx;
+  if (!make_tmap(&tw, w1_fp4, (uint64_t)K / 2, (uint64_t)E * 2 * I, 64)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tx, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kChunk)) return MOE_ERR_CUDA;
+  Params p{};
+  p.a_sf = a_sf;
+  p.w_sf = w1_sf;
+  p.offsets = offsets;
+  p.padded_offsets = padded_offsets;
+  p.E = E;
+  p.Kred = K;
+  p.n_tiles = I / 64;
+  p.w_rows = 2 * I;
+  p.I = I;
+  p.gs_a = gs_a;
+  p.gs_w0 = gs_g;
+  p.gs_w1 = gs_u;
+  p.out_bf16 = out_bf16;
+  p.out_ld = epilogue == MOE_L1_GATEUP_BF16 ? 2 * (int64_t)I : I;
+  p.h_amax = h_amax;
+  p.h_fp4 = h_fp4;
+  p.h_sf = h_sf;
+  p.gs_h = gs_h;
+  p.cap = cap;
+  p.status = status;
+  if (epilogue == MOE_L1_SILU_BF16 && h_amax && cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  switch (epilogue) {
+    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(tw, tx, p, st);
+    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(tw, tx, p, st);
+    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(tw, tx, p, st);
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
+                                 const int32_t* padded_offsets, int E, int64_t cap, int I, int K,
+                                 const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2, int epilogue,
+                                 void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
+                                 int64_t T, int32_t* status, cudaStream_t st) {
+  using namespace stream;
+  CUtensorMap tw, tx;
+  if (!make_tmap(&tw, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, 128)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tx, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kChunk)) return MOE_ERR_CUDA;
+  Params p{};
+  p.a_sf = h_sf;
+  p.w_sf = w2_sf;
+  p.offsets = offsets;
+  p.padded_offsets = padded_offsets;
+  p.E = E;
+  p.Kred = I;
+  p.n_tiles = K / 128;
+  p.w_rows = K;
+  p.I = I;
+  p.gs_a = gs_h;
+  p.gs_w0 = gs_w2;
+  p.out_bf16 = y_rows;
+  p.out_ld = K;
+  p.slot_token = slot_token;
+  p.slot_weight = slot_weight;
+  p.out32 = out32;
+  p.T = T;
+  p.out_cols = K;
+  p.cap = cap;
+  p.status = status;
+  switch (epilogue) {
+    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(tw, tx, p, st);
+    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(tw, tx, p, st);
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+}  // namespace moe

@@ -60,4 +60,22 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
                           const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
                           int32_t* status, cudaStream_t st);
 
+// ---- gemm_stream.cu (weight-streaming kernel for small per-expert slot counts) ----
+bool stream_gemm_supported(int Kred);
+moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,
+                                 const int32_t* padded_offsets, int E, int64_t cap, int K, int I,
+                                 const uint8_t* w1_fp4, const uint8_t* w1_sf, const float* gs_g, const float* gs_u,
+                                 int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4, uint8_t* h_sf,
+                                 const float* gs_h, int32_t* status, cudaStream_t st);
+moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
+                                 const int32_t* padded_offsets, int E, int64_t cap, int I, int K,
+                                 const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2, int epilogue,
+                                 void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
+                                 int64_t T, int32_t* status, cudaStream_t st);
+
+// Which grouped-GEMM kernel runs (process-wide; moe_set_gemm_policy).
+int gemm_policy();
+int set_gemm_policy(int policy);
+bool use_stream_gemm(int64_t cap, int E, int Kred);
+
 }  // namespace moe

@@ -21,6 +21,15 @@ def _lib():
     B, R = binding, runtime
 
 
+@pytest.fixture(params=["tiled", "streaming"], autouse=True)
+def gemm_kernel(request, _lib):
+    """Run every test with each grouped-GEMM kernel forced."""
+    pol = {"tiled": B.MOE_GEMM_TILED, "streaming": B.MOE_GEMM_STREAMING}[request.param]
+    old = B.moe_set_gemm_policy(pol)
+    yield request.param
+    B.moe_set_gemm_policy(old)
+
+
 def _layer(W, wl):
     return R.layer_from_nvfp4(W["w1_codes"], W["w1_sf"], W["gs_w1_gate"], W["gs_w1_up"], W["w2_codes"],
                               W["w2_sf"], W["gs_w2"], wl.topk, wl.expert_offset)

@@ -83,15 +83,29 @@ def _gpu_forward(layer, wl, mode, gs_h=None):
     return out.float().cpu().numpy(), float(fw.gs_h.item()), x, ids, w
 
 
-def test_decode_every_token_dynamic_and_fixed(layer, full_weights):
+@pytest.fixture(scope="module")
+def decode_ref(full_weights):
     wl = workloads.WORKLOADS["decode"]
-    got_dyn, gs_dyn, x, ids, w = _gpu_forward(layer, wl, B.MOE_GS_DYNAMIC)
-    ref = omoe.forward(x.float().numpy(), ids, w, wl.E, wl.expert_offset, full_weights)
-    assert_layer_close(got_dyn, ref["out"], "decode dynamic")
-    assert abs(gs_dyn - float(ref["gs_h"])) <= 1e-3 * float(ref["gs_h"])
-    # the calibrated mode bench.py times: the h scale held fixed at the data-derived value
-    got_fix, _, _, _, _ = _gpu_forward(layer, wl, B.MOE_GS_FIXED, gs_h=ref["gs_h"])
-    assert_layer_close(got_fix, ref["out"], "decode fixed")
+    x = workloads.activations(wl)
+    ids, w = workloads.routing(wl)
+    return omoe.forward(x.float().numpy(), ids, w, wl.E, wl.expert_offset, full_weights)
+
+
+@pytest.mark.parametrize("policy", ["auto", "tiled"])
+def test_decode_every_token_dynamic_and_fixed(layer, decode_ref, policy):
+    """auto picks the weight-streaming kernel for this workload; tiled forces the other."""
+    wl = workloads.WORKLOADS["decode"]
+    old = B.moe_set_gemm_policy(B.MOE_GEMM_AUTO if policy == "auto" else B.MOE_GEMM_TILED)
+    try:
+        got_dyn, gs_dyn, x, ids, w = _gpu_forward(layer, wl, B.MOE_GS_DYNAMIC)
+        ref = decode_ref
+        assert_layer_close(got_dyn, ref["out"], "decode dynamic")
+        assert abs(gs_dyn - float(ref["gs_h"])) <= 1e-3 * float(ref["gs_h"])
+        # the calibrated mode bench.py times: the h scale held fixed at the data-derived value
+        got_fix, _, _, _, _ = _gpu_forward(layer, wl, B.MOE_GS_FIXED, gs_h=ref["gs_h"])
+        assert_layer_close(got_fix, ref["out"], "decode fixed")
+    finally:
+        B.moe_set_gemm_policy(old)
 
 
 def _sampled(layer, full_weights, wl, tokens):

@@ -24,6 +24,15 @@ def _lib():
     B = binding
 
 
+@pytest.fixture(params=["tiled", "streaming"], autouse=True)
+def gemm_kernel(request, _lib):
+    """Run every test with each grouped-GEMM kernel forced."""
+    pol = {"tiled": B.MOE_GEMM_TILED, "streaming": B.MOE_GEMM_STREAMING}[request.param]
+    old = B.moe_set_gemm_policy(pol)
+    yield request.param
+    B.moe_set_gemm_policy(old)
+
+
 POW2_BYTES = np.array([0x28, 0x30, 0x38, 0x40, 0x48], np.uint8)  # 0.25 .. 4
 POW2_BYTES_NARROW = np.array([0x30, 0x38, 0x40], np.uint8)       # 0.5 .. 2
 
