@@ -32,7 +32,7 @@ constexpr int kStages = 6;
 constexpr int kWStage = 128 * 128;            // 16 KB: 128 weight rows x 256 fp4
 constexpr int kBStage = kChunk * 128;         // 8 KB: 64 slot rows x 256 fp4
 constexpr int kSfwStage = 4 * 512;            // 4 weight-scale atoms
-constexpr int kThreads = 224;                 // 7 warps
+constexpr int kThreads = 256;                 // 8 warps
 constexpr int kTmemCols = 512;
 constexpr int kMaxKSteps = 64;                // contraction <= 4096
 constexpr int kSfbBase = 2 * kChunk;          // 128: two accumulators of 64 columns first
@@ -81,10 +81,11 @@ struct __align__(1024) Smem {
   uint16_t xu[kChunk][kStageLd];    //              up values
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t drain;
-  uint64_t fin;
+  uint64_t tfull;                   // both issuers' MMAs of a tile done (2 arrivals)
+  uint64_t tempty;                  // epilogue has the accumulators in registers (4 warps)
+  uint64_t drain[2];                // issuer r's MMAs so far done (one arrival per chunk switch)
+  uint64_t fin[2];
+  uint64_t sfb_ready;               // the chunk's activation scales are in TMEM
   uint64_t img_full;
   uint64_t img_free;
   uint32_t tmem_base;
@@ -148,12 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
+    mbar_init(&s.tfull, 2);
+    mbar_init(&s.tempty, 4);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);
+      mbar_init(&s.drain[i], 1);
+      mbar_init(&s.fin[i], 1);
     }
-    mbar_init(&s.drain, 1);
-    mbar_init(&s.fin, 1);
+    mbar_init(&s.sfb_ready, 1);
     mbar_init(&s.img_full, 1);
     mbar_init(&s.img_free, 1);
     s.abort_flag = 0;
@@ -219,37 +221,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kStages; ++i)
           if (issued[i]) wait_bar_drain(&s.full[i], issued_phase[i]);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 7) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads issue concurrently (the tensor pipe serves each issuing thread at
+    // roughly one instruction per ~130 cycles): issuer r takes the k-blocks with
+    // kb % 2 == r of every tile and accumulates into its own 64 columns; the
+    // epilogue adds the two partial sums.  Issuer 0 also owns the resident
+    // activation scales.
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      const int r = warp == 1 ? 0 : 1;
       bool ok = true;
       int it = 0, ch = -1, last_e = -1, last_c = -1;
+      uint32_t g = 0;  // k-blocks of earlier tiles (ring position)
       Cursor cur;
-      for (int t = t_lo; t < t_hi && ok; ++t, ++it) {
+      for (int t = t_lo; t < t_hi && ok; ++t, ++it, g += nkb) {
         int c, n;
         cur.locate(s, p.n_tiles, t, c, n);
         if (cur.e != last_e || c != last_c) {
-          // new chunk: let the MMAs reading the old activation scales finish, then
-          // copy the new chunk's scale images into TMEM
           ++ch;
           last_e = cur.e;
           last_c = c;
-          if (ch > 0) {
-            tc_commit(&s.drain);
-            if (!wait_bar_bounded(&s.drain, (ch - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (r == 0) {
+            // both issuers' MMAs reading the old scales must finish before they are replaced
+            if (ch > 0) {
+              tc_commit(&s.drain[0]);
+              if (!wait_bar_bounded(&s.drain[0], (ch - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+              if (!wait_bar_bounded(&s.drain[1], (ch - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+            }
+            if (!wait_bar_bounded(&s.img_full, ch & 1, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            for (int k = 0; k < ksf4; ++k) tc_cp_sf(tmem + kSfbBase + 4 * k, sdesc_sf(s.img[k]));
+            tc_commit(&s.img_free);
+            tc_commit(&s.sfb_ready);
+          } else {
+            if (ch > 0) tc_commit(&s.drain[1]);
+            if (!wait_bar_bounded(&s.sfb_ready, ch & 1, abort_flag, p.status)) { ok = false; break; }
           }
-          if (!wait_bar_bounded(&s.img_full, ch & 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          for (int k = 0; k < ksf4; ++k) tc_cp_sf(tmem + kSfbBase + 4 * k, sdesc_sf(s.img[k]));
-          tc_commit(&s.img_free);
         }
-        const int acc = it & 1;
-        if (!wait_bar_bounded(&s.tempty[acc], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + acc * kChunk;
-        for (int kb = 0; kb < nkb; ++kb) {
+        const uint32_t d = tmem + r * kChunk;
+        bool first = true;
+        for (int kb = r; kb < nkb; kb += 2) {
+          const uint32_t gs = g + kb;
+          const int stage = gs % kStages;
+          const uint32_t phase = (gs / kStages) & 1;
           const int natoms = min(4, ksf4 - 4 * kb);
           if (!wait_bar_bounded(&s.full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
@@ -257,15 +273,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int a = 0; a < natoms; ++a) tc_cp_sf(sfw_col + 4 * a, sdesc_sf(s.sfw[stage] + 512 * a));
           for (int kk = 0; kk < natoms; ++kk)
             tc_mma_fp4(d, sdesc_sw128(s.w[stage] + 32 * kk), sdesc_sw128(s.b[stage] + 32 * kk), kIdesc,
-                       sfw_col + 4 * kk, tmem + kSfbBase + 4 * (4 * kb + kk), (kb | kk) != 0);
+                       sfw_col + 4 * kk, tmem + kSfbBase + 4 * (4 * kb + kk), (!first || kk > 0) ? 1u : 0u);
           tc_commit(&s.empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          first = false;
         }
         if (!ok) break;
-        tc_commit(&s.tfull[acc]);
+        tc_commit(&s.tfull);  // arrives once this issuer's MMAs of the tile are done
       }
-      tc_commit(&s.fin);
-      wait_bar_drain(&s.fin, 0);
+      tc_commit(&s.fin[r]);
+      wait_bar_drain(&s.fin[r], 0);
     }
   } else if (warp == 6) {
     // ------------------------------------------------------------ activation-scale images
@@ -304,18 +320,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c, n;
       cur.locate(s, p.n_tiles, t, c, n);
       const int e = cur.e;
-      const int acc = it & 1;
-      wait_bar_bounded(&s.tfull[acc], (it >> 1) & 1, abort_flag, p.status);
+      wait_bar_bounded(&s.tfull, it & 1, abort_flag, p.status);
       epi_bar();  // every epilogue warp has arrived (and sees an abort set before)
       if (*(volatile int*)abort_flag) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kChunk;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
       float v[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; j += 16) tmem_ld16(taddr + j, *reinterpret_cast<float(*)[16]>(&v[j]));
+      if (nkb > 1) {  // partial sum of the odd k-blocks
+#pragma unroll
+        for (int j = 0; j < kChunk; j += 16) {
+          float y[16];
+          tmem_ld16(taddr + kChunk + j, y);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[j + i] = __fadd_rn(v[j + i], y[i]);
+        }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.tempty[acc]);  // accumulator free: values are in registers
+      if (lane == 0) mbar_arrive(&s.tempty);  // accumulators free: values are in registers
 
       const int cnt_c = min(kChunk, s.cnt[e] - c * kChunk);  // valid slots of this chunk
       const int64_t row0 = (int64_t)s.poff[e] + c * kChunk;
