@@ -76,8 +76,6 @@ moe_status amax_launch(const void* x, int64_t rows, int K, int64_t ld_x, uint32_
 moe_status route_impl(const int32_t* ids, const float* w, int64_t T, int topk, int E, int off, int32_t* counts,
                       int32_t* offsets, int32_t* poff, int32_t* slot_token, float* slot_weight, int32_t* pair_slot,
                       int64_t capacity, int32_t* cnt, int32_t* base, int32_t* status, cudaStream_t st) {
-  if (cudaMemsetAsync(slot_token, 0xFF, capacity * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(slot_weight, 0, capacity * sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
   const int nchunks = (int)route_chunks(T, topk);
   return launch_route(ids, w, T * topk, topk, E, off, cnt, base, nchunks, counts, offsets, poff, slot_token,
                       slot_weight, pair_slot, capacity, status, st) == cudaSuccess

@@ -15,7 +15,10 @@
 //   * each CTA walks a contiguous range of (expert, chunk, weight-block) tiles, so
 //     consecutive tiles reuse the resident activation scales;
 //   * warp 6 builds the TMEM images of the next chunk's activation scales in shared
-//     memory while the current chunk runs.
+//     memory while the current chunk runs;
+//   * two MMA-issuing warps split every tile's k-blocks by parity into two
+//     accumulators (the epilogue adds them), since the tensor pipe serves each
+//     issuing thread at about one instruction per ~130 cycles.
 //
 // Scale-factor placement read by kind::mxf4nvf4.block_scale.scale_vec::4X (M=128):
 // operand A row m at TMEM lane m, column base + m/32; operand B row n at lane n%32,
@@ -85,7 +88,6 @@ struct __align__(1024) Smem {
   uint64_t tempty;                  // epilogue has the accumulators in registers (4 warps)
   uint64_t drain[2];                // issuer r's MMAs so far done (one arrival per chunk switch)
   uint64_t fin[2];
-  uint64_t sfb_ready;               // the chunk's activation scales are in TMEM
   uint64_t img_full;
   uint64_t img_free;
   uint32_t tmem_base;
@@ -155,9 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.drain[i], 1);
       mbar_init(&s.fin[i], 1);
     }
-    mbar_init(&s.sfb_ready, 1);
     mbar_init(&s.img_full, 1);
-    mbar_init(&s.img_free, 1);
+    mbar_init(&s.img_free, 2);
     s.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -226,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Two threads issue concurrently (the tensor pipe serves each issuing thread at
     // roughly one instruction per ~130 cycles): issuer r takes the k-blocks with
     // kb % 2 == r of every tile and accumulates into its own 64 columns; the
-    // epilogue adds the two partial sums.  Issuer 0 also owns the resident
-    // activation scales.
+    // epilogue adds the two partial sums.  Each issuer copies the resident
+    // activation scales of its own k-blocks during the first tile of a chunk.
     if (lane == 0) {
       const int r = warp == 1 ? 0 : 1;
       bool ok = true;
@@ -237,26 +238,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = t_lo; t < t_hi && ok; ++t, ++it, g += nkb) {
         int c, n;
         cur.locate(s, p.n_tiles, t, c, n);
+        bool fresh = false;  // first tile of a chunk: copy this issuer's activation scales
         if (cur.e != last_e || c != last_c) {
           ++ch;
           last_e = cur.e;
           last_c = c;
-          if (r == 0) {
-            // both issuers' MMAs reading the old scales must finish before they are replaced
-            if (ch > 0) {
-              tc_commit(&s.drain[0]);
-              if (!wait_bar_bounded(&s.drain[0], (ch - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-              if (!wait_bar_bounded(&s.drain[1], (ch - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-            }
-            if (!wait_bar_bounded(&s.img_full, ch & 1, abort_flag, p.status)) { ok = false; break; }
-            tc_fence_after();
-            for (int k = 0; k < ksf4; ++k) tc_cp_sf(tmem + kSfbBase + 4 * k, sdesc_sf(s.img[k]));
-            tc_commit(&s.img_free);
-            tc_commit(&s.sfb_ready);
-          } else {
-            if (ch > 0) tc_commit(&s.drain[1]);
-            if (!wait_bar_bounded(&s.sfb_ready, ch & 1, abort_flag, p.status)) { ok = false; break; }
+          fresh = true;
+          // this issuer's MMAs reading its old scale columns must finish first; the
+          // other issuer never reads them (k-blocks are split by parity)
+          if (ch > 0) {
+            tc_commit(&s.drain[r]);
+            if (!wait_bar_bounded(&s.drain[r], (ch - 1) & 1, abort_flag, p.status)) { ok = false; break; }
           }
+          if (!wait_bar_bounded(&s.img_full, ch & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
         }
         if (!wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -271,6 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sfw_col = tmem + kSfwBase + 16 * stage;
           for (int a = 0; a < natoms; ++a) tc_cp_sf(sfw_col + 4 * a, sdesc_sf(s.sfw[stage] + 512 * a));
+          if (fresh)
+            for (int a = 0; a < natoms; ++a)
+              tc_cp_sf(tmem + kSfbBase + 4 * (4 * kb + a), sdesc_sf(s.img[4 * kb + a]));
           for (int kk = 0; kk < natoms; ++kk)
             tc_mma_fp4(d, sdesc_sw128(s.w[stage] + 32 * kk), sdesc_sw128(s.b[stage] + 32 * kk), kIdesc,
                        sfw_col + 4 * kk, tmem + kSfbBase + 4 * (4 * kb + kk), (!first || kk > 0) ? 1u : 0u);
@@ -278,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           first = false;
         }
         if (!ok) break;
+        if (fresh) tc_commit(&s.img_free);  // images may be rebuilt once both issuers' copies are done
         tc_commit(&s.tfull);  // arrives once this issuer's MMAs of the tile are done
       }
       tc_commit(&s.fin[r]);
@@ -300,10 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t r1 = r0 + 32;
       const uint8_t* base0 = p.a_sf + (r0 >> 7) * (int64_t)ksf4 * 512 + (r0 & 31) * 16 + ((r0 >> 5) & 3) * 4;
       const uint8_t* base1 = p.a_sf + (r1 >> 7) * (int64_t)ksf4 * 512 + (r1 & 31) * 16 + ((r1 >> 5) & 3) * 4;
-      for (int k = 0; k < ksf4; ++k) {
-        const uint32_t s0 = __ldg(reinterpret_cast<const uint32_t*>(base0 + k * 512));
-        const uint32_t s1 = __ldg(reinterpret_cast<const uint32_t*>(base1 + k * 512));
-        *reinterpret_cast<uint4*>(&s.img[k][lane * 16]) = make_uint4(s0, s1, 0u, 0u);
+      for (int k0 = 0; k0 < ksf4; k0 += 8) {
+        uint32_t s0[8], s1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (k0 + j < ksf4) {
+            s0[j] = __ldg(reinterpret_cast<const uint32_t*>(base0 + (k0 + j) * 512));
+            s1[j] = __ldg(reinterpret_cast<const uint32_t*>(base1 + (k0 + j) * 512));
+          }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (k0 + j < ksf4) *reinterpret_cast<uint4*>(&s.img[k0 + j][lane * 16]) = make_uint4(s0[j], s1[j], 0u, 0u);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();

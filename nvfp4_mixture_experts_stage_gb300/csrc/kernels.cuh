@@ -43,6 +43,8 @@ constexpr int kRouteChunk = 256;  // pairs per warp
 constexpr int kRouteWarps = 8;    // warps per block (count / place)
 constexpr int kMaxExperts = 256;
 
+// Routes the pairs and initialises every slot of [0, capacity) (padding: token -1,
+// weight 0); one single-block kernel up to 8192 pairs, count/scan/place above.
 cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk, int E, int off, int32_t* cnt,
                          int32_t* base, int nchunks, int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
                          int32_t* slot_token, float* slot_weight, int32_t* pair_slot, int64_t capacity,

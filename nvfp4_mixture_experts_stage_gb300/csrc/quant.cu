@@ -102,6 +102,15 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
       v[u] = ok ? __ldcs(a.x + row[u] * a.ld_vec + (col[u] >> 3)) : make_uint4(0, 0, 0, 0);
       if (!ok) col[u] = -1;
     }
+    // slots of each segment's token, fetched up front so the loads overlap (top-k <= 8)
+    int32_t ps[U][8];
+    if (DST == kDstSlots && a.topk <= 8) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          ps[u][j] = (col[u] >= 0 && j < a.topk) ? __ldg(a.pair_slot + row[u] * a.topk + j) : -1;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
@@ -131,13 +140,17 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
       const bool sf_lane = (lane & 7) == 0;
       const int ks = col[u] >> 4;  // scale column of this lane's block
       if (DST == kDstSlots) {
-        for (int j = 0; j < a.topk; ++j) {
-          const int32_t p = __ldg(a.pair_slot + row[u] * a.topk + j);
-          if (p < 0) continue;
-          if (p >= a.capacity) { set_status(a.status, MOE_ERR_DEVICE_INDEX); continue; }
+        auto put = [&](int32_t p) {
+          if (p < 0) return;
+          if (p >= a.capacity) { set_status(a.status, MOE_ERR_DEVICE_INDEX); return; }
           *reinterpret_cast<uint32_t*>(a.codes + (int64_t)p * half_k + (col[u] >> 1)) = code;
-          if (sf_lane)
-            *reinterpret_cast<uint32_t*>(a.sf + sf_swizzle_offset(p, ks, k_sf)) = sfw;
+          if (sf_lane) *reinterpret_cast<uint32_t*>(a.sf + sf_swizzle_offset(p, ks, k_sf)) = sfw;
+        };
+        if (a.topk <= 8) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) put(ps[u][j]);
+        } else {
+          for (int j = 0; j < a.topk; ++j) put(__ldg(a.pair_slot + row[u] * a.topk + j));
         }
       } else {
         *reinterpret_cast<uint32_t*>(a.codes + row[u] * half_k + (col[u] >> 1)) = code;

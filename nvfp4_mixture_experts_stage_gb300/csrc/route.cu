@@ -138,10 +138,147 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_place_kernel(
   }
 }
 
+// Whole routing in one block of 32 warps for up to kSmallRoutePairs pairs (decode
+// batches): warp w owns the contiguous pairs [w*G*32, (w+1)*G*32) in groups of 32,
+// counts them per expert, a per-expert scan over the 32 warps gives each warp its
+// first rank, a scan over experts gives the offsets, then the warps place their
+// pairs in order (stable) and the block fills the padding slots.
+constexpr int kSmallRoutePairs = 8192;
+constexpr int kSmallGroups = kSmallRoutePairs / (32 * 32);  // 32-pair groups per warp (max)
+
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int P, int topk, int E, int off,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
+    int32_t* __restrict__ slot_token, float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot,
+    int64_t capacity, int32_t* status) {
+  extern __shared__ int sm[];
+  int* wcnt = sm;                  // [32][E] per-warp counts, then per-warp running slot
+  __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = (P + 1023) / 1024;  // groups per warp
+  for (int i = threadIdx.x; i < 32 * E; i += 1024) wcnt[i] = 0;
+  int loc[kSmallGroups];
+  float wt[kSmallGroups];
+#pragma unroll
+  for (int g = 0; g < kSmallGroups; ++g) {
+    const int idx = (warp * G + g) * 32 + lane;
+    const bool in = g < G && idx < P;
+    loc[g] = in ? local_expert(ids, idx, P, off, E) : -1;
+    wt[g] = in ? __ldg(w + idx) : 0.0f;
+  }
+  __syncthreads();
+  int* mine = wcnt + warp * E;
+#pragma unroll
+  for (int g = 0; g < kSmallGroups; ++g) {
+    if (g >= G) break;
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, loc[g]);
+    if (loc[g] >= 0 && lane == __ffs(grp) - 1) mine[loc[g]] += __popc(grp);
+    __syncwarp();
+  }
+  __syncthreads();
+  // per expert: exclusive scan over the 32 warps (warp-parallel over experts)
+  for (int e = warp; e < E; e += 32) {
+    const int v = wcnt[lane * E + e];
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += t;
+    }
+    wcnt[lane * E + e] = incl - v;
+    if (lane == 31) s_cnt[e] = incl;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0, prun = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? s_cnt[e] : 0;
+      const int pv = (v + kTileM - 1) / kTileM * kTileM;
+      int incl = v, pincl = pv;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        const int pt = __shfl_up_sync(0xFFFFFFFFu, pincl, d);
+        if (lane >= d) { incl += t; pincl += pt; }
+      }
+      if (e < E) {
+        s_off[e] = run + incl - v;
+        s_poff[e] = prun + pincl - pv;
+      }
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      prun += __shfl_sync(0xFFFFFFFFu, pincl, 31);
+    }
+    if (lane == 0) {
+      s_off[E] = run;
+      s_poff[E] = prun;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += 1024) {
+    if (e < E) counts[e] = s_cnt[e];
+    offsets[e] = s_off[e];
+    padded_offsets[e] = s_poff[e];
+  }
+  // place: running slot of (warp, expert) = padded offset + ranks of earlier warps
+  for (int e = lane; e < E; e += 32) mine[e] += s_poff[e];
+  __syncwarp();
+  const unsigned lower = (1u << lane) - 1u;
+#pragma unroll
+  for (int g = 0; g < kSmallGroups; ++g) {
+    if (g >= G) break;
+    const int idx = (warp * G + g) * 32 + lane;
+    const int l = loc[g];
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, l);
+    int slot = -1;
+    if (l >= 0) slot = mine[l] + __popc(grp & lower);
+    __syncwarp();
+    if (l >= 0 && lane == __ffs(grp) - 1) mine[l] += __popc(grp);
+    __syncwarp();
+    if (idx < P) {
+      if (slot >= capacity) {
+        set_status(status, MOE_ERR_DEVICE_INDEX);
+        slot = -1;
+      }
+      pair_slot[idx] = slot;
+      if (slot >= 0) {
+        slot_token[slot] = idx / topk;
+        slot_weight[slot] = wt[g];
+      }
+    }
+  }
+  // padding slots: the tail of each expert's padded range, then everything past the last
+  for (int e = warp; e < E; e += 32)
+    for (int p = s_poff[e] + s_cnt[e] + lane; p < s_poff[e + 1] && p < capacity; p += 32) {
+      slot_token[p] = -1;
+      slot_weight[p] = 0.0f;
+    }
+  for (int64_t p = s_poff[E] + threadIdx.x; p < capacity; p += 1024) {
+    slot_token[p] = -1;
+    slot_weight[p] = 0.0f;
+  }
+}
+
 cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk, int E, int off, int32_t* cnt,
                          int32_t* base, int nchunks, int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
                          int32_t* slot_token, float* slot_weight, int32_t* pair_slot, int64_t capacity,
                          int32_t* status, cudaStream_t st) {
+  if (P <= kSmallRoutePairs) {
+    static bool configured = false;
+    const int smem = 32 * kMaxExperts * (int)sizeof(int);
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    route_small_kernel<<<1, 1024, 32 * E * sizeof(int), st>>>(ids, w, (int)P, topk, E, off, counts, offsets,
+                                                              padded_offsets, slot_token, slot_weight, pair_slot,
+                                                              capacity, status);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaMemsetAsync(slot_token, 0xFF, capacity * sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(slot_weight, 0, capacity * sizeof(float), st);
+  if (e != cudaSuccess) return e;
   const int blocks = (nchunks + kRouteWarps - 1) / kRouteWarps;
   if (nchunks > 0) route_count_kernel<<<blocks, kRouteWarps * 32, 0, st>>>(ids, P, E, off, cnt, nchunks);
   route_scan_kernel<<<1, 1024, 0, st>>>(cnt, nchunks, E, base, counts, offsets, padded_offsets);

@@ -61,8 +61,6 @@ extern "C" moe_status moe_route_static_scratch(const int32_t* topk_ids, const fl
   int32_t* cnt = scratch;
   int32_t* base = scratch + kStaticTableInts;
   cudaStream_t st = stream;
-  if (cudaMemsetAsync(slot_token, 0xFF, capacity * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(slot_weight, 0, capacity * sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
   return moe::launch_route(topk_ids, topk_w, T * topk, topk, E, expert_offset, cnt, base, (int)nchunks, counts,
                            offsets, padded_offsets, slot_token, slot_weight, pair_slot, capacity, nullptr, st) ==
                  cudaSuccess
