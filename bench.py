@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-policy", default="auto", choices=["auto", "tiled", "stream", "stream32", "stream64"],
+                    help="grouped-GEMM kernel selection (moe_set_gemm_policy)")
     ap.add_argument("--profile-only", action="store_true",
                     help="run warm-up + steps of the fixed-gs layer and exit (for ncu); prints nothing")
     return ap.parse_args()
@@ -203,7 +205,7 @@ def timed_steps(fw, x, ids, w, steps, warmup, flush, ws):
     t0 = time.perf_counter()
     step_ms, rows = [], []
     for _ in range(steps):
-        flush.zero_()                       # write 2x L2 between steps: every step starts cold
+        flush.sum()                         # read 2x L2 between steps: every step starts cold (and clean)
         graph.replay()
         torch.cuda.synchronize()
         step_ms.append(evs[0].elapsed_time(evs[6]))
@@ -268,6 +270,9 @@ def run_ours(args, ws, rank, local):
     build.build()
     from nvfp4_mixture_experts_stage_gb300 import binding as B, runtime as R
 
+    B.moe_set_gemm_policy({"auto": B.MOE_GEMM_AUTO, "tiled": B.MOE_GEMM_TILED, "stream": B.MOE_GEMM_STREAMING,
+                           "stream32": B.MOE_GEMM_STREAMING_N32,
+                           "stream64": B.MOE_GEMM_STREAMING_N64}[args.gemm_policy])
     wl = workloads.WORKLOADS[args.workload]
     torch.manual_seed(0)
     x_c = workloads.activations(wl)
@@ -350,8 +355,10 @@ def run_ours(args, ws, rank, local):
                                f"{wl.expert_offset}), top-{wl.topk} uniform",
                    "tokens_per_step": wl.T, "local_slots": alg["S"], "experts_touched": alg["touched"],
                    "gs_h": "fixed (calibrated in warm-up)", "gs_x": "dynamic (amax every step)",
-                   "l2": "flushed (256 MB write) between timed steps; weights 1.02 GB > L2",
+                   "l2": "inputs larger than L2 (weights 1.02 GB streamed every step) and L2 flushed between timed steps by "
+                         "reading a 256 MB buffer (a read flush leaves no dirty lines to write back in the timed region)",
                    "launch": "each step one CUDA-graph replay of moe_forward",
+                   "gemm_policy": args.gemm_policy,
                    "parallelism": f"replicas x{ws}"},
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "gemm_tflops": gemm_tflops,

@@ -265,15 +265,20 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const 
  *   MOE_GEMM_TILED     always the tiled kernel: 128 slot rows x 128 weight rows per
  *                      tile, slots on the MMA's M side;
  *   MOE_GEMM_STREAMING the weight-streaming kernel whenever the contraction is
- *                      <= 4096: weight rows on the MMA's M side, chunks of up to 64
- *                      slots on its N side, the chunk's activation scales resident
- *                      in tensor memory.  Experts with more than 64 slots are split
- *                      into several chunks, each streaming the expert's weights.
+ *                      <= 4096: weight rows on the MMA's M side, chunks of slots on
+ *                      its N side, the chunk's activation scales resident in tensor
+ *                      memory.  Experts with more slots than a chunk are split
+ *                      into several chunks; an expert's chunks are processed back to
+ *                      back for each weight block, so the repeated weight reads come
+ *                      from L2.  The chunk is 32 slots (8 pipeline stages fit);
+ *   MOE_GEMM_STREAMING_N32 / _N64  the streaming kernel with the chunk forced.
  * Both kernels compute the same arithmetic (results may differ in the fp32
  * summation order only). */
-#define MOE_GEMM_AUTO      0
-#define MOE_GEMM_TILED     1
-#define MOE_GEMM_STREAMING 2
+#define MOE_GEMM_AUTO           0
+#define MOE_GEMM_TILED          1
+#define MOE_GEMM_STREAMING      2
+#define MOE_GEMM_STREAMING_N32  3
+#define MOE_GEMM_STREAMING_N64  4
 int moe_set_gemm_policy(int policy);
 
 /* out_bf16[i] = bf16(out32[i]) for i < T*K (round to nearest even). */

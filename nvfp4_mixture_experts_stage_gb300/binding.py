@@ -41,6 +41,7 @@ EXPORTS = (
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
+MOE_GEMM_STREAMING_N32, MOE_GEMM_STREAMING_N64 = 3, 4
 
 MOE_ROUTE_STATIC_TABLE_INTS = 262144
 

@@ -402,9 +402,13 @@ int set_gemm_policy(int policy) { return __atomic_exchange_n(&g_policy, policy, 
 bool use_stream_gemm(int64_t cap, int E, int Kred) {
   const int pol = gemm_policy();
   if (pol == MOE_GEMM_TILED || !stream_gemm_supported(Kred)) return false;
-  if (pol == MOE_GEMM_STREAMING) return true;
+  if (pol != MOE_GEMM_AUTO) return true;
   return cap - (int64_t)(kTileM - 1) * E <= (int64_t)64 * E;
 }
+
+// Slot chunk of the streaming kernel: 32 (more pipeline stages fit; heavier experts
+// take several chunks) unless the policy forces 64.
+int stream_chunk(int64_t, int) { return gemm_policy() == MOE_GEMM_STREAMING_N64 ? 64 : 32; }
 
 // L1: A = slot activations [cap, K/2]; B = W1 [E*2I, K/2]; N per tile = 64 h cols.
 moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,

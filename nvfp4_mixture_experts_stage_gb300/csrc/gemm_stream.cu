@@ -30,20 +30,24 @@
 namespace moe {
 namespace stream {
 
-constexpr int kChunk = 64;                    // slots per chunk (MMA N)
-constexpr int kStages = 6;
+// CHUNK = slots per chunk (the MMA's N): 32 or 64.  A 32-slot chunk halves the
+// activation tile and leaves room for 8 pipeline stages instead of 6.
+template <int CHUNK>
+struct Cfg {
+  static constexpr int kStages = CHUNK == 32 ? 8 : 6;
+  static constexpr int kBStage = CHUNK * 128;            // CHUNK slot rows x 256 fp4
+  static constexpr int kSfbBase = 2 * CHUNK;             // two accumulators of CHUNK columns first
+  static constexpr int kSfwBase = kSfbBase + 4 * 64;     // resident activation scales: 4 columns per k-step
+  static constexpr uint32_t kIdesc =
+      (1u << 7) | (1u << 10) | ((uint32_t)(CHUNK >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  static_assert(kSfwBase + 16 * kStages <= 512, "tensor memory budget");
+};
 constexpr int kWStage = 128 * 128;            // 16 KB: 128 weight rows x 256 fp4
-constexpr int kBStage = kChunk * 128;         // 8 KB: 64 slot rows x 256 fp4
 constexpr int kSfwStage = 4 * 512;            // 4 weight-scale atoms
 constexpr int kThreads = 256;                 // 8 warps
 constexpr int kTmemCols = 512;
 constexpr int kMaxKSteps = 64;                // contraction <= 4096
-constexpr int kSfbBase = 2 * kChunk;          // 128: two accumulators of 64 columns first
-constexpr int kSfwBase = kSfbBase + 4 * kMaxKSteps;  // 384; stage s at 384 + 16 s (< 480)
 constexpr int kStageLd = 72;                  // padded row of the L1 exchange buffers (bf16)
-
-constexpr uint32_t kIdesc =
-    (1u << 7) | (1u << 10) | ((uint32_t)(kChunk >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 
 enum Kind : int { kL1GateUp = 0, kL1Silu = 1, kL1Requant = 2, kL2Rows = 3, kL2Scatter = 4 };
 
@@ -75,13 +79,15 @@ struct Params {
   int32_t* status;
 };
 
+template <int CHUNK>
 struct __align__(1024) Smem {
+  static constexpr int kStages = Cfg<CHUNK>::kStages;
   uint8_t w[kStages][kWStage];
-  uint8_t b[kStages][kBStage];
+  uint8_t b[kStages][Cfg<CHUNK>::kBStage];
   uint8_t sfw[kStages][kSfwStage];
   uint8_t img[kMaxKSteps][512];
-  uint16_t xg[kChunk][kStageLd];    // L1 exchange: gate values [slot][h col] (bf16 bits)
-  uint16_t xu[kChunk][kStageLd];    //              up values
+  uint16_t xg[CHUNK][kStageLd];     // L1 exchange: gate values [slot][h col] (bf16 bits)
+  uint16_t xu[CHUNK][kStageLd];     //              up values
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull;                   // both issuers' MMAs of a tile done (2 arrivals)
@@ -98,25 +104,38 @@ struct __align__(1024) Smem {
   int cum[257];                     // tiles before expert e
 };
 
-// Tile t -> (expert, chunk, weight block); e advances monotonically with t.
+// Tile t -> (expert, chunk, weight block); e advances monotonically with t.  Within
+// an expert the chunk varies fastest, so an expert split into several chunks reads
+// each weight block again right after the first read (from L2).
+template <int CHUNK>
 struct Cursor {
   int e = 0;
-  MOE_DEV void locate(const Smem& s, int n_tiles, int t, int& c, int& n) {
+  template <class S>
+  MOE_DEV void locate(const S& s, int n_tiles, int t, int& c, int& n) {
     while (t >= s.cum[e + 1]) ++e;
     const int local = t - s.cum[e];
-    c = local / n_tiles;
-    n = local - c * n_tiles;
+    const int nch = (s.cnt[e] + CHUNK - 1) / CHUNK;
+    n = local / nch;
+    c = local - n * nch;
   }
 };
 
 MOE_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <int KIND>
+template <int KIND, int CHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
     stream_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                        const Params p) {
+  using C = Cfg<CHUNK>;
+  constexpr int kChunk = CHUNK;
+  constexpr int kStages = C::kStages;
+  constexpr int kBStage = C::kBStage;
+  constexpr int kSfbBase = C::kSfbBase;
+  constexpr int kSfwBase = C::kSfwBase;
+  constexpr uint32_t kIdesc = C::kIdesc;
   extern __shared__ uint8_t smem_raw[];
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem<CHUNK>& s =
+      *reinterpret_cast<Smem<CHUNK>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool kL1 = KIND <= kL1Requant;
 
@@ -192,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[kStages];
       for (int i = 0; i < kStages; ++i) issued[i] = false;
       bool ok = true;
-      Cursor cur;
+      Cursor<CHUNK> cur;
       for (int t = t_lo; t < t_hi && ok; ++t) {
         int c, n;
         cur.locate(s, p.n_tiles, t, c, n);
@@ -234,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int it = 0, ch = -1, last_e = -1, last_c = -1;
       uint32_t g = 0;  // k-blocks of earlier tiles (ring position)
-      Cursor cur;
+      Cursor<CHUNK> cur;
       for (int t = t_lo; t < t_hi && ok; ++t, ++it, g += nkb) {
         int c, n;
         cur.locate(s, p.n_tiles, t, c, n);
@@ -285,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 6) {
     // ------------------------------------------------------------ activation-scale images
     int ch = -1, last_e = -1, last_c = -1;
-    Cursor cur;
+    Cursor<CHUNK> cur;
     for (int t = t_lo; t < t_hi; ++t) {
       int c, n;
       cur.locate(s, p.n_tiles, t, c, n);
@@ -296,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar_bounded(&s.img_free, (ch & 1) ^ 1, abort_flag, p.status)) break;
       // image row i (16 B): scales of chunk rows i and 32+i for k-step k, then zeros
       const int64_t r0 = (int64_t)s.poff[cur.e] + c * kChunk + lane;
-      const int64_t r1 = r0 + 32;
+      const int64_t r1 = kChunk == 64 ? r0 + 32 : r0;  // (a 32-slot chunk uses byte group 0 only)
       const uint8_t* base0 = p.a_sf + (r0 >> 7) * (int64_t)ksf4 * 512 + (r0 & 31) * 16 + ((r0 >> 5) & 3) * 4;
       const uint8_t* base1 = p.a_sf + (r1 >> 7) * (int64_t)ksf4 * 512 + (r1 & 31) * 16 + ((r1 >> 5) & 3) * 4;
       for (int k0 = 0; k0 < ksf4; k0 += 8) {
@@ -309,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (k0 + j < ksf4) *reinterpret_cast<uint4*>(&s.img[k0 + j][lane * 16]) = make_uint4(s0[j], s1[j], 0u, 0u);
+          if (k0 + j < ksf4)
+            *reinterpret_cast<uint4*>(&s.img[k0 + j][lane * 16]) = make_uint4(s0[j], kChunk == 64 ? s1[j] : 0u, 0u, 0u);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -320,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;           // TMEM lane quarter = weight rows 32q..32q+31
     const int tid = threadIdx.x - 64; // 0..127 over the four epilogue warps
     int it = 0;
-    Cursor cur;
+    Cursor<CHUNK> cur;
     float amax = 0.0f;
     for (int t = t_lo; t < t_hi; ++t, ++it) {
       int c, n;
@@ -359,15 +379,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kChunk; ++j)
           if (j < cnt_c) x[j][col] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(alpha, v[j])));
         epi_bar();  // exchange complete
-        const int sl = tid >> 1, hb = tid & 1;  // slot, 32-column half
+        // thread -> (slot, part): 128 threads over CHUNK slots x 64 columns; each part is
+        // NB 16-column blocks
+        constexpr int kParts = 128 / kChunk;      // 2 (64-slot chunk) or 4 (32-slot chunk)
+        constexpr int NB = 4 / kParts;            // 2 or 1 blocks per thread
+        constexpr int NC = 16 * NB;               // 32 or 16 columns per thread
+        const int sl = tid / kParts, hb = tid % kParts;
         if (sl < cnt_c) {
           const int64_t prow = row0 + sl;
-          const int hcol = n * 64 + hb * 32;
-          float g[32], u[32];
+          const int hcol = n * 64 + hb * NC;
+          float g[NC], u[NC];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const uint32_t gw = *reinterpret_cast<const uint32_t*>(&s.xg[sl][hb * 32 + i]);
-            const uint32_t uw = *reinterpret_cast<const uint32_t*>(&s.xu[sl][hb * 32 + i]);
+          for (int i = 0; i < NC; i += 2) {
+            const uint32_t gw = *reinterpret_cast<const uint32_t*>(&s.xg[sl][hb * NC + i]);
+            const uint32_t uw = *reinterpret_cast<const uint32_t*>(&s.xu[sl][hb * NC + i]);
             g[i] = bf16lo(gw); g[i + 1] = bf16hi(gw);
             u[i] = bf16lo(uw); u[i + 1] = bf16hi(uw);
           }
@@ -375,29 +400,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4* dg = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + hcol);
             uint4* du = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + p.I + hcol);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < NC / 8; ++i) {
               dg[i] = make_uint4(pack_bf16x2(g[8 * i], g[8 * i + 1]), pack_bf16x2(g[8 * i + 2], g[8 * i + 3]),
                                  pack_bf16x2(g[8 * i + 4], g[8 * i + 5]), pack_bf16x2(g[8 * i + 6], g[8 * i + 7]));
               du[i] = make_uint4(pack_bf16x2(u[8 * i], u[8 * i + 1]), pack_bf16x2(u[8 * i + 2], u[8 * i + 3]),
                                  pack_bf16x2(u[8 * i + 4], u[8 * i + 5]), pack_bf16x2(u[8 * i + 6], u[8 * i + 7]));
             }
           } else {
-            float h[32];
+            float h[NC];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = silu_mul(g[i], u[i]);
+            for (int i = 0; i < NC; ++i) h[i] = silu_mul(g[i], u[i]);
             if (KIND == kL1Silu) {
               uint4* dh = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + hcol);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
+              for (int i = 0; i < NC / 8; ++i)
                 dh[i] = make_uint4(pack_bf16x2(h[8 * i], h[8 * i + 1]), pack_bf16x2(h[8 * i + 2], h[8 * i + 3]),
                                    pack_bf16x2(h[8 * i + 4], h[8 * i + 5]), pack_bf16x2(h[8 * i + 6], h[8 * i + 7]));
 #pragma unroll
-              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+              for (int i = 0; i < NC; ++i) amax = fmaxf(amax, fabsf(h[i]));
             } else {
               const float rg = recip_global_scale(__ldg(p.gs_h));
-              uint32_t sfw = 0, cw[4];
+              uint32_t sfw = 0, cw[2 * NB];
 #pragma unroll
-              for (int b = 0; b < 2; ++b) {  // two 16-element blocks
+              for (int b = 0; b < NB; ++b) {  // 16-element blocks
                 float bm = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(h[16 * b + i]));
@@ -416,8 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                   cw[2 * b + w4] = word;
                 }
               }
-              *reinterpret_cast<uint4*>(p.h_fp4 + prow * (p.I >> 1) + (hcol >> 1)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-              *reinterpret_cast<uint16_t*>(p.h_sf + sf_swizzle_offset(prow, hcol >> 4, p.I >> 4)) = (uint16_t)sfw;
+              uint8_t* hp = p.h_fp4 + prow * (p.I >> 1) + (hcol >> 1);
+              uint8_t* sp = p.h_sf + sf_swizzle_offset(prow, hcol >> 4, p.I >> 4);
+              if (NB == 2) {
+                *reinterpret_cast<uint4*>(hp) = make_uint4(cw[0], cw[1], cw[2 % (2 * NB)], cw[3 % (2 * NB)]);
+                *reinterpret_cast<uint16_t*>(sp) = (uint16_t)sfw;
+              } else {
+                *reinterpret_cast<uint2*>(hp) = make_uint2(cw[0], cw[1]);
+                *sp = (uint8_t)sfw;
+              }
             }
           }
         }
@@ -458,19 +490,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-
-template <int KIND>
-static moe_status launch_kind(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, cudaStream_t st) {
+template <int KIND, int CHUNK>
+static moe_status launch_chunk(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, cudaStream_t st) {
+  constexpr size_t kSmemBytes = sizeof(Smem<CHUNK>) + 1024;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(stream_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(stream_gemm_kernel<KIND, CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return MOE_ERR_CUDA;
     configured = true;
   }
-  stream_gemm_kernel<KIND><<<num_sms(), kThreads, kSmemBytes, st>>>(tw, tx, p);
+  stream_gemm_kernel<KIND, CHUNK><<<num_sms(), kThreads, kSmemBytes, st>>>(tw, tx, p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <int KIND>
+static moe_status launch_kind(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, int chunk,
+                              cudaStream_t st) {
+  return chunk == 32 ? launch_chunk<KIND, 32>(tw, tx, p, st) : launch_chunk<KIND, 64>(tw, tx, p, st);
 }
 
 }  // namespace stream
@@ -483,9 +520,10 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
                                  int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4, uint8_t* h_sf,
                                  const float* gs_h, int32_t* status, cudaStream_t st) {
   using namespace stream;
+  const int chunk = stream_chunk(cap, E);
   CUtensorMap tw, tx;
   if (!make_tmap(&tw, w1_fp4, (uint64_t)K / 2, (uint64_t)E * 2 * I, 64)) return MOE_ERR_CUDA;
-  if (!make_tmap(&tx, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kChunk)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tx, a_fp4, (uint64_t)K / 2, (uint64_t)cap, chunk)) return MOE_ERR_CUDA;
   Params p{};
   p.a_sf = a_sf;
   p.w_sf = w1_sf;
@@ -510,9 +548,9 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
   if (epilogue == MOE_L1_SILU_BF16 && h_amax && cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
     return MOE_ERR_CUDA;
   switch (epilogue) {
-    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(tw, tx, p, st);
-    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(tw, tx, p, st);
-    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(tw, tx, p, st);
+    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(tw, tx, p, chunk, st);
+    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(tw, tx, p, chunk, st);
+    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(tw, tx, p, chunk, st);
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -523,9 +561,10 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
                                  void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
                                  int64_t T, int32_t* status, cudaStream_t st) {
   using namespace stream;
+  const int chunk = stream_chunk(cap, E);
   CUtensorMap tw, tx;
   if (!make_tmap(&tw, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, 128)) return MOE_ERR_CUDA;
-  if (!make_tmap(&tx, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kChunk)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tx, h_fp4, (uint64_t)I / 2, (uint64_t)cap, chunk)) return MOE_ERR_CUDA;
   Params p{};
   p.a_sf = h_sf;
   p.w_sf = w2_sf;
@@ -548,8 +587,8 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
   p.cap = cap;
   p.status = status;
   switch (epilogue) {
-    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(tw, tx, p, st);
-    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(tw, tx, p, st);
+    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(tw, tx, p, chunk, st);
+    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(tw, tx, p, chunk, st);
   }
   return MOE_ERR_INVALID_ARG;
 }

@@ -79,5 +79,6 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
 int gemm_policy();
 int set_gemm_policy(int policy);
 bool use_stream_gemm(int64_t cap, int E, int Kred);
+int stream_chunk(int64_t cap, int E);
 
 }  // namespace moe

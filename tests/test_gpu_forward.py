@@ -21,10 +21,11 @@ def _lib():
     B, R = binding, runtime
 
 
-@pytest.fixture(params=["tiled", "streaming"], autouse=True)
+@pytest.fixture(params=["tiled", "stream32", "stream64"], autouse=True)
 def gemm_kernel(request, _lib):
-    """Run every test with each grouped-GEMM kernel forced."""
-    pol = {"tiled": B.MOE_GEMM_TILED, "streaming": B.MOE_GEMM_STREAMING}[request.param]
+    """Run every test with each grouped-GEMM kernel (and streaming chunk) forced."""
+    pol = {"tiled": B.MOE_GEMM_TILED, "stream32": B.MOE_GEMM_STREAMING_N32,
+           "stream64": B.MOE_GEMM_STREAMING_N64}[request.param]
     old = B.moe_set_gemm_policy(pol)
     yield request.param
     B.moe_set_gemm_policy(old)
