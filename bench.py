@@ -185,33 +185,50 @@ STAGES = ["route", "stage_x", "gemm_l1", "requant", "gemm_l2", "cast"]
 KERNELS_PER_STEP = {"fixed": 8, "dynamic": 9}  # count, scan, place, amax, quantize, l1, [requant], l2, cast
 
 
+def _capture(fw, x, ids, w, events):
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fw(x, ids, w, events=events)
+    return graph
+
+
 def timed_steps(fw, x, ids, w, steps, warmup, flush, ws):
-    """Time `steps` calls of the layer, each replayed from one CUDA graph (the
-    layer's launches, the stage-boundary event records included) after an L2
-    flush; the device time of each step comes from its captured events."""
+    """Time `steps` calls of the layer, each a replay of one captured CUDA graph
+    of moe_forward after an L2 flush.
+
+    Two loops over the same call: the step times come from a graph with events
+    at the start and the end only; the per-stage times (and the L1 kernel time
+    used for the roofline) from a graph that also records the five stage
+    boundaries -- every event-record node adds a few microseconds to the step,
+    so those stages sum to more than the step."""
     for _ in range(warmup):
         fw(x, ids, w)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
     for e in evs:
         e.record()
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        fw(x, ids, w, events=evs)
+    g_ends = _capture(fw, x, ids, w, [evs[0], None, None, None, None, None, evs[6]])
+    g_stages = _capture(fw, x, ids, w, evs)
     for _ in range(warmup):
-        graph.replay()
+        g_ends.replay()
+        g_stages.replay()
     torch.cuda.synchronize()
     barrier(ws)
     t0 = time.perf_counter()
-    step_ms, rows = [], []
+    step_ms = []
     for _ in range(steps):
         flush.sum()                         # read 2x L2 between steps: every step starts cold (and clean)
-        graph.replay()
+        g_ends.replay()
         torch.cuda.synchronize()
         step_ms.append(evs[0].elapsed_time(evs[6]))
-        rows.append([evs[j].elapsed_time(evs[j + 1]) for j in range(6)])
     barrier(ws)
     wall = time.perf_counter() - t0
+    rows = []
+    for _ in range(steps):
+        flush.sum()
+        g_stages.replay()
+        torch.cuda.synchronize()
+        rows.append([evs[j].elapsed_time(evs[j + 1]) for j in range(6)])
     rows = np.array(rows)
     stage_ms = {n: float(rows[:, j].mean()) for j, n in enumerate(STAGES)}
     return np.array(step_ms), stage_ms, wall
@@ -357,7 +374,8 @@ def run_ours(args, ws, rank, local):
                    "gs_h": "fixed (calibrated in warm-up)", "gs_x": "dynamic (amax every step)",
                    "l2": "inputs larger than L2 (weights 1.02 GB streamed every step) and L2 flushed between timed steps by "
                          "reading a 256 MB buffer (a read flush leaves no dirty lines to write back in the timed region)",
-                   "launch": "each step one CUDA-graph replay of moe_forward",
+                   "launch": "each step one CUDA-graph replay of moe_forward (events at start and end only); "
+                             "stage_ms from a second loop whose graph also records the stage boundaries",
                    "gemm_policy": args.gemm_policy,
                    "parallelism": f"replicas x{ws}"},
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},

@@ -240,10 +240,11 @@ def moe_forward(x, topk_ids, topk_w, E, I, expert_offset, weights, gs_h_mode, gs
 def moe_forward_traced(x, topk_ids, topk_w, E, I, expert_offset, weights, gs_h_mode, gs_h, out, ws, events,
                        gs_x_fixed=None, dev_status=None, stream=None):
     """moe_forward that records MOE_TRACE_EVENTS torch.cuda.Event objects (timing
-    enabled, already created by one record()) at the stage boundaries."""
+    enabled, already created by one record()) at the stage boundaries; None
+    entries are skipped."""
     T, K = x.shape
     topk = topk_ids.shape[1]
-    arr = (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[ev.cuda_event for ev in events])
+    arr = (ctypes.c_void_p * MOE_TRACE_EVENTS)(*[None if ev is None else ev.cuda_event for ev in events])
     _check("moe_forward_traced", _lib.moe_forward_traced(
         _p(x), T, K, I, E, _p(topk_ids), _p(topk_w), topk, expert_offset, ctypes.byref(weights),
         _p(gs_x_fixed), gs_h_mode, _p(gs_h), _p(out), _p(dev_status), _p(ws), ws.numel() * ws.element_size(),

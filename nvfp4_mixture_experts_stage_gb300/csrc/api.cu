@@ -42,13 +42,16 @@ struct Carve {
 moe_status quantize_launch(int dst, const void* x, int64_t rows, int K, int64_t ld_x, const uint32_t* amax_bits,
                            const float* gs_fixed, float* gs_out, uint8_t* codes, uint8_t* sf,
                            const int32_t* pair_slot, int topk, const int32_t* slot_token, int64_t capacity,
-                           int32_t* status, cudaStream_t st) {
+                           int32_t* status, cudaStream_t st, const uint32_t* amax_partials = nullptr,
+                           int n_partials = 0) {
   QuantArgs a;
   a.x = reinterpret_cast<const uint4*>(x);
   a.rows = rows;
   a.K = K;
   a.ld_vec = ld_x / 8;
   a.amax_bits = amax_bits;
+  a.amax_partials = amax_partials;
+  a.n_partials = n_partials;
   a.gs_fixed = gs_fixed;
   a.gs_out = gs_out;
   a.codes = codes;
@@ -135,7 +138,7 @@ size_t moe_stage_workspace_size(void) { return 256; }
 
 static size_t forward_layout(Carve& c, int64_t T, int K, int I, int E, int topk, void** parts) {
   const int64_t cap = moe_slot_capacity(T, topk, E);
-  parts[0] = c.take<uint32_t>(64);                                   // scalars
+  parts[0] = c.take<uint32_t>(512);                                  // scalars, amax partials
   parts[1] = c.take<uint8_t>(moe_route_workspace_size(T, topk, E));  // route tables
   parts[2] = c.take<int32_t>(E);                                     // counts
   parts[3] = c.take<int32_t>(E + 1);                                 // offsets
@@ -343,16 +346,49 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
 
   moe_status s;
   if (mark(stage_events, 0, stream) != MOE_OK) return MOE_ERR_CUDA;
-  if (cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
-  s = route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, poff, slot_token, slot_weight,
-                 pair_slot, cap, rcnt, rbase, dev_status, stream);
-  if (s != MOE_OK || (s = mark(stage_events, 1, stream)) != MOE_OK) return s;
-  if (!gs_x_fixed) {
-    s = amax_launch(x, T, K, K, x_amax, stream);
-    if (s != MOE_OK) return s;
+  if (T * topk <= kSmallRoutePairsMax) {
+    // one launch: routing (block 0) + per-block amax of x + zeroing of out32
+    uint32_t* partials = scal + 256;
+    const int64_t vecs = T * (K / 8), n4 = T * K / 4;
+    const int nb = (int)std::min<int64_t>(std::max<int64_t>(ceil_div(std::max(vecs, n4), 2048), 1), 256);
+    PrologueArgs pa;
+    pa.ids = topk_ids;
+    pa.w = topk_w;
+    pa.P = (int)(T * topk);
+    pa.topk = topk;
+    pa.E = E;
+    pa.off = expert_offset;
+    pa.counts = counts;
+    pa.offsets = offsets;
+    pa.padded_offsets = poff;
+    pa.slot_token = slot_token;
+    pa.slot_weight = slot_weight;
+    pa.pair_slot = pair_slot;
+    pa.capacity = cap;
+    pa.status = dev_status;
+    pa.x = reinterpret_cast<const uint4*>(x);
+    pa.rows = T;
+    pa.vec_per_row = K / 8;
+    pa.ld_vec = K / 8;
+    pa.amax_partials = gs_x_fixed ? nullptr : partials;
+    pa.out32 = out32;
+    pa.out32_n4 = n4;
+    if (launch_forward_prologue(pa, nb, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((s = mark(stage_events, 1, stream)) != MOE_OK) return s;
+    s = quantize_launch(2, x, T, K, K, nullptr, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk, nullptr, cap,
+                        dev_status, stream, gs_x_fixed ? nullptr : partials, nb);
+  } else {
+    if (cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    s = route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, poff, slot_token, slot_weight,
+                   pair_slot, cap, rcnt, rbase, dev_status, stream);
+    if (s != MOE_OK || (s = mark(stage_events, 1, stream)) != MOE_OK) return s;
+    if (!gs_x_fixed) {
+      s = amax_launch(x, T, K, K, x_amax, stream);
+      if (s != MOE_OK) return s;
+    }
+    s = quantize_launch(2, x, T, K, K, gs_x_fixed ? nullptr : x_amax, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot,
+                        topk, nullptr, cap, dev_status, stream);
   }
-  s = quantize_launch(2, x, T, K, K, gs_x_fixed ? nullptr : x_amax, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk,
-                      nullptr, cap, dev_status, stream);
   if (s != MOE_OK || (s = mark(stage_events, 2, stream)) != MOE_OK) return s;
   if (gs_h_mode == MOE_GS_DYNAMIC) {
     s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,

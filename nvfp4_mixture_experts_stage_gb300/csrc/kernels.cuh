@@ -19,6 +19,8 @@ struct QuantArgs {
   int K;                      // elements per row (multiple of 64)
   int64_t ld_vec;             // row stride in 16-byte vectors
   const uint32_t* amax_bits;  // dynamic: fp32 bits of max|x|  (or NULL)
+  const uint32_t* amax_partials;  // dynamic: per-block maxima (fp32 bits) to reduce (or NULL)
+  int n_partials;
   const float* gs_fixed;      // fixed global scale (or NULL)
   float* gs_out;              // written by one thread (or NULL)
   uint8_t* codes;
@@ -49,6 +51,30 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk
                          int32_t* base, int nchunks, int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
                          int32_t* slot_token, float* slot_weight, int32_t* pair_slot, int64_t capacity,
                          int32_t* status, cudaStream_t st);
+
+// Small-batch start of the layer: routing + amax partials + zeroing out32, one launch.
+constexpr int kSmallRoutePairsMax = 8192;
+struct PrologueArgs {
+  const int32_t* ids;
+  const float* w;
+  int P, topk, E, off;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* padded_offsets;
+  int32_t* slot_token;
+  float* slot_weight;
+  int32_t* pair_slot;
+  int64_t capacity;
+  int32_t* status;
+  const uint4* x;            // activations (16-byte vectors)
+  int64_t rows;
+  int vec_per_row;
+  int64_t ld_vec;
+  uint32_t* amax_partials;   // [amax_blocks] fp32 bits, or NULL (fixed global scale)
+  float* out32;
+  int64_t out32_n4;          // float4 count to zero
+};
+cudaError_t launch_forward_prologue(const PrologueArgs& a, int amax_blocks, cudaStream_t st);
 
 // ---- gemm.cu ----
 moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,

@@ -72,8 +72,17 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint4* __restrict_
 // ---------------------------------------------------------------------------
 template <int DST>
 __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
-  const float gs = a.gs_fixed ? __ldg(a.gs_fixed)
-                              : __fdiv_rn(__uint_as_float(*a.amax_bits), kGsDivisor);
+  float amax_f = 0.0f;
+  if (!a.gs_fixed) {
+    if (a.amax_partials) {  // reduce the per-block maxima (non-negative: bits order like values)
+      uint32_t m = 0;
+      for (int i = threadIdx.x & 31; i < a.n_partials; i += 32) m = max(m, __ldg(a.amax_partials + i));
+      amax_f = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, m));
+    } else {
+      amax_f = __uint_as_float(*a.amax_bits);
+    }
+  }
+  const float gs = a.gs_fixed ? __ldg(a.gs_fixed) : __fdiv_rn(amax_f, kGsDivisor);
   const float rg = recip_global_scale(gs);
   if (a.gs_out && blockIdx.x == 0 && threadIdx.x == 0) *a.gs_out = gs;
 

@@ -146,13 +146,12 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_place_kernel(
 constexpr int kSmallRoutePairs = 8192;
 constexpr int kSmallGroups = kSmallRoutePairs / (32 * 32);  // 32-pair groups per warp (max)
 
-__global__ void __launch_bounds__(1024) route_small_kernel(
+// One block of 1024 threads; wcnt: 32*E ints of shared memory.
+__device__ __forceinline__ void route_small_block(
     const int32_t* __restrict__ ids, const float* __restrict__ w, int P, int topk, int E, int off,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
     int32_t* __restrict__ slot_token, float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot,
-    int64_t capacity, int32_t* status) {
-  extern __shared__ int sm[];
-  int* wcnt = sm;                  // [32][E] per-warp counts, then per-warp running slot
+    int64_t capacity, int32_t* status, int* wcnt) {
   __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (P + 1023) / 1024;  // groups per warp
@@ -257,6 +256,69 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     slot_token[p] = -1;
     slot_weight[p] = 0.0f;
   }
+}
+
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int P, int topk, int E, int off,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
+    int32_t* __restrict__ slot_token, float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot,
+    int64_t capacity, int32_t* status) {
+  extern __shared__ int sm[];
+  route_small_block(ids, w, P, topk, E, off, counts, offsets, padded_offsets, slot_token, slot_weight, pair_slot,
+                    capacity, status, sm);
+}
+
+// The start of the layer for small batches, in one launch: block 0 routes (as
+// route_small_kernel); the other blocks take the per-block max |x| (written to
+// amax_partials[block-1], no atomics, so nothing has to be cleared first) and zero
+// the fp32 output accumulator.
+__global__ void __launch_bounds__(1024) forward_prologue_kernel(PrologueArgs a) {
+  extern __shared__ int sm[];
+  if (blockIdx.x == 0) {
+    route_small_block(a.ids, a.w, a.P, a.topk, a.E, a.off, a.counts, a.offsets, a.padded_offsets, a.slot_token,
+                      a.slot_weight, a.pair_slot, a.capacity, a.status, sm);
+    return;
+  }
+  const uint32_t nb = gridDim.x - 1, b = blockIdx.x - 1;
+  const uint32_t stride = nb * blockDim.x;
+  // zero out32 (float4 stores)
+  float4* o = reinterpret_cast<float4*>(a.out32);
+  for (int64_t i = (int64_t)b * blockDim.x + threadIdx.x; i < a.out32_n4; i += stride) o[i] = make_float4(0, 0, 0, 0);
+  if (!a.amax_partials) return;
+  // max |x| over this block's share of the 16-byte vectors
+  const uint32_t vpr = (uint32_t)a.vec_per_row;
+  const uint32_t total = (uint32_t)(a.rows * a.vec_per_row);
+  uint32_t m = 0;
+  for (uint32_t v = b * blockDim.x + threadIdx.x; v < total; v += stride) {
+    const uint32_t r = v / vpr;
+    const uint4 q = __ldg(a.x + (int64_t)r * a.ld_vec + (v - r * vpr));
+    m = __vmaxu2(m, q.x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, q.y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, q.z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, q.w & 0x7FFF7FFFu);
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t red[32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (threadIdx.x == 0) a.amax_partials[b] = v << 16;  // bf16 magnitude -> fp32 bits
+  }
+}
+
+cudaError_t launch_forward_prologue(const PrologueArgs& a, int amax_blocks, cudaStream_t st) {
+  static bool configured = false;
+  const int smem = 32 * kMaxExperts * (int)sizeof(int);
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(forward_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  forward_prologue_kernel<<<1 + amax_blocks, 1024, 32 * a.E * sizeof(int), st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk, int E, int off, int32_t* cnt,
