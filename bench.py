@@ -37,14 +37,14 @@ import workloads  # noqa: E402
 METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 peak"
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture
-# (profiles/gemm_l1_decode.md), valid only for the GEMM sources it was taken on.
-NCU_TRAFFIC = {"gemm_l1": {"bytes": 683280640, "sources_sha256_16": "b05ab368a9fe582f"}}
+# (profiles/gemm_l1_stream_decode.md), valid only for the GEMM sources it was taken on.
+NCU_TRAFFIC = {"gemm_l1": {"bytes": 674900480, "sources_sha256_16": "4e3bbbea97188e6f"}}
 
 
 def gemm_sources_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm.cu", "kernels.cuh", "common.cuh"):
+    for f in ("gemm.cu", "gemm_stream.cu", "tcgen05.cuh", "kernels.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_stage_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
