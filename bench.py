@@ -182,7 +182,16 @@ def algorithmic(wl, counts):
 
 
 STAGES = ["route", "stage_x", "gemm_l1", "requant", "gemm_l2", "cast"]
-KERNELS_PER_STEP = {"fixed": 8, "dynamic": 9}  # count, scan, place, amax, quantize, l1, [requant], l2, cast
+SMALL_ROUTE_PAIRS_MAX = 8192   # moe_forward's one-launch prologue covers T*topk up to this many pairs
+
+
+def kernels_per_step(T, topk, dynamic_h):
+    """Kernels one moe_forward launches (x's scale derived from the data, as timed here).
+
+    T*topk <= 8192: prologue (routing + amax partials + output zeroing), quantize, L1, [requant], L2, cast.
+    Above: count, scan, place, amax, quantize, L1, [requant], L2, cast (the memsets are copies, not kernels)."""
+    n = 5 if T * topk <= SMALL_ROUTE_PAIRS_MAX else 8
+    return n + (1 if dynamic_h else 0)
 
 
 def _capture(fw, x, ids, w, events):
@@ -389,7 +398,7 @@ def run_ours(args, ws, rank, local):
         "e2e": {"value": wl.T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4,
                 "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": e2e_ms},
-        "gpu_launches": KERNELS_PER_STEP["fixed"] * args.steps,
+        "gpu_launches": kernels_per_step(wl.T, wl.topk, False) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

@@ -43,7 +43,7 @@ moe_status quantize_launch(int dst, const void* x, int64_t rows, int K, int64_t 
                            const float* gs_fixed, float* gs_out, uint8_t* codes, uint8_t* sf,
                            const int32_t* pair_slot, int topk, const int32_t* slot_token, int64_t capacity,
                            int32_t* status, cudaStream_t st, const uint32_t* amax_partials = nullptr,
-                           int n_partials = 0) {
+                           int n_partials = 0, bool pdl = false) {
   QuantArgs a;
   a.x = reinterpret_cast<const uint4*>(x);
   a.rows = rows;
@@ -64,7 +64,7 @@ moe_status quantize_launch(int dst, const void* x, int64_t rows, int K, int64_t 
   const int64_t warps = rows * ceil_div(K, 256);
   if (warps >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   int blocks = (int)std::min<int64_t>(std::max<int64_t>(ceil_div(warps, 8 * 4), 1), (int64_t)sm_count() * 8);
-  return launch_quantize(dst, a, blocks, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_quantize(dst, a, blocks, st, pdl) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status amax_launch(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, cudaStream_t st) {
@@ -87,6 +87,15 @@ moe_status route_impl(const int32_t* ids, const float* w, int64_t T, int topk, i
 }
 
 // Record stage event i (if any); inside a graph capture it becomes a record node.
+moe_status cast_output(const float* out32, void* out_bf16, int64_t T, int K, cudaStream_t stream, bool pdl) {
+  if (T < 0 || K <= 0 || K % 8) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!out32 || !out_bf16 || !aligned(out32, 16) || !aligned(out_bf16, 16)) return MOE_ERR_INVALID_ARG;
+  const int64_t n8 = T * K / 8;
+  const int blocks = (int)std::min<int64_t>(ceil_div(n8, 256), (int64_t)sm_count() * 8);
+  return launch_cast(out32, out_bf16, n8, blocks, stream, pdl) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 moe_status mark(void* const* events, int i, cudaStream_t st) {
   if (!events || !events[i]) return MOE_OK;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -290,12 +299,7 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const 
 }
 
 moe_status moe_cast_output(const float* out32, void* out_bf16, int64_t T, int K, moe_stream_t stream) {
-  if (T < 0 || K <= 0 || K % 8) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return MOE_OK;
-  if (!out32 || !out_bf16 || !aligned(out32, 16) || !aligned(out_bf16, 16)) return MOE_ERR_INVALID_ARG;
-  const int64_t n8 = T * K / 8;
-  const int blocks = (int)std::min<int64_t>(ceil_div(n8, 256), (int64_t)sm_count() * 8);
-  return launch_cast(out32, out_bf16, n8, blocks, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return cast_output(out32, out_bf16, T, K, stream, false);
 }
 
 moe_status moe_forward(const void* x, int64_t T, int K, int I, int E, const int32_t* topk_ids, const float* topk_w,
@@ -345,6 +349,11 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
   float* out32 = reinterpret_cast<float*>(parts[13]);
 
   moe_status s;
+  // Kernels after the first run as programmatic dependents of their predecessor (each
+  // waits for it before touching its results, and may start early) unless stage
+  // events are recorded between them (events 0 and 6 sit outside the kernel chain).
+  bool pdl = true;
+  for (int i = 1; stage_events && i < 6; ++i) pdl = pdl && stage_events[i] == nullptr;
   if (mark(stage_events, 0, stream) != MOE_OK) return MOE_ERR_CUDA;
   if (T * topk <= kSmallRoutePairsMax) {
     // one launch: routing (block 0) + per-block amax of x + zeroing of out32
@@ -375,8 +384,10 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     pa.out32_n4 = n4;
     if (launch_forward_prologue(pa, nb, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if ((s = mark(stage_events, 1, stream)) != MOE_OK) return s;
+    // Not a programmatic dependent: launched early, its blocks would be placed on the
+    // few SMs the prologue leaves free and run there several times slower.
     s = quantize_launch(2, x, T, K, K, nullptr, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk, nullptr, cap,
-                        dev_status, stream, gs_x_fixed ? nullptr : partials, nb);
+                        dev_status, stream, gs_x_fixed ? nullptr : partials, nb, false);
   } else {
     if (cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
     s = route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, poff, slot_token, slot_weight,
@@ -387,25 +398,27 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
       if (s != MOE_OK) return s;
     }
     s = quantize_launch(2, x, T, K, K, gs_x_fixed ? nullptr : x_amax, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot,
-                        topk, nullptr, cap, dev_status, stream);
+                        topk, nullptr, cap, dev_status, stream, nullptr, 0, pdl);
   }
   if (s != MOE_OK || (s = mark(stage_events, 2, stream)) != MOE_OK) return s;
   if (gs_h_mode == MOE_GS_DYNAMIC) {
     s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
-                       w->gs_w1_up, MOE_L1_SILU_BF16, h_bf16, h_amax, nullptr, nullptr, nullptr, dev_status, stream);
+                       w->gs_w1_up, MOE_L1_SILU_BF16, h_bf16, h_amax, nullptr, nullptr, nullptr, dev_status, stream,
+                       pdl);
     if (s != MOE_OK || (s = mark(stage_events, 3, stream)) != MOE_OK) return s;
     s = quantize_launch(3, h_bf16, cap, I, I, reinterpret_cast<const uint32_t*>(h_amax), nullptr, gs_h, h_fp4, h_sf,
-                        nullptr, 0, slot_token, cap, dev_status, stream);
+                        nullptr, 0, slot_token, cap, dev_status, stream, nullptr, 0, pdl);
   } else {
     s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
-                       w->gs_w1_up, MOE_L1_SILU_REQUANT, nullptr, nullptr, h_fp4, h_sf, gs_h, dev_status, stream);
+                       w->gs_w1_up, MOE_L1_SILU_REQUANT, nullptr, nullptr, h_fp4, h_sf, gs_h, dev_status, stream,
+                       pdl);
     if (s != MOE_OK || (s = mark(stage_events, 3, stream)) != MOE_OK) return s;
   }
   if (s != MOE_OK || (s = mark(stage_events, 4, stream)) != MOE_OK) return s;
   s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2, MOE_L2_SCATTER,
-                     nullptr, slot_token, slot_weight, out32, T, dev_status, stream);
+                     nullptr, slot_token, slot_weight, out32, T, dev_status, stream, pdl);
   if (s != MOE_OK || (s = mark(stage_events, 5, stream)) != MOE_OK) return s;
-  s = moe_cast_output(out32, out, T, K, stream);
+  s = cast_output(out32, out, T, K, stream, pdl);
   if (s != MOE_OK) return s;
   return mark(stage_events, 6, stream);
 }

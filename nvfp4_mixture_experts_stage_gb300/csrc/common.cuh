@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -15,6 +16,30 @@ namespace moe {
 constexpr int kTileM = 128;
 constexpr int kBlock = 16;              // elements per block scale
 constexpr float kGsDivisor = 2688.0f;   // 6 * 448
+
+// Programmatic dependent launch.  A kernel launched with launch_ex(..., pdl=true)
+// may start while the previous kernel of the stream is still running:
+// griddep_wait() blocks until that kernel has completed and its writes are
+// visible; griddep_launch_dependents() lets the next such kernel start early.
+// Both are no-ops for a kernel launched without the attribute.
+MOE_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // First error wins.
 MOE_DEV void set_status(int32_t* status, int code) {

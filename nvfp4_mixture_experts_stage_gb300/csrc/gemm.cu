@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool kL1 = KIND <= kL1Requant;
 
+  griddep_wait();
+  griddep_launch_dependents();
   if (threadIdx.x == 0) s.bad_offsets = 0;
   __syncthreads();
   for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.poff[i] = p.padded_offsets[i];
@@ -379,7 +381,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 constexpr size_t kGemmSmemBytes = sizeof(GemmSmem) + 1024;
 
 template <int KIND>
-static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st) {
+static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st,
+                              bool pdl) {
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -387,8 +390,10 @@ static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, cons
       return MOE_ERR_CUDA;
     configured = true;
   }
-  grouped_gemm_kernel<KIND><<<num_sms(), kGemmThreads, kGemmSmemBytes, st>>>(ta, tb, p);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_ex(grouped_gemm_kernel<KIND>, num_sms(), kGemmThreads, kGemmSmemBytes, st, pdl, ta, tb, p) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 static int g_policy = MOE_GEMM_AUTO;
@@ -415,10 +420,10 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
                           const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
                           const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
                           float* h_amax, uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h, int32_t* status,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool pdl) {
   if (use_stream_gemm(cap, E, K))
     return launch_stream_gemm_l1(a_fp4, a_sf, gs_a, offsets, padded_offsets, E, cap, K, I, w1_fp4, w1_sf, gs_g, gs_u,
-                                 epilogue, out_bf16, h_amax, h_fp4, h_sf, gs_h, status, st);
+                                 epilogue, out_bf16, h_amax, h_fp4, h_sf, gs_h, status, st, pdl);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w1_fp4, (uint64_t)K / 2, (uint64_t)E * 2 * I, 64)) return MOE_ERR_CUDA;
@@ -443,12 +448,14 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
   p.h_sf = h_sf;
   p.gs_h = gs_h;
   p.status = status;
-  if (epilogue == MOE_L1_SILU_BF16 && h_amax && cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (epilogue == MOE_L1_SILU_BF16 && h_amax) {
+    if (cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
+    pdl = false;  // the predecessor is now the memset, not a kernel
+  }
   switch (epilogue) {
-    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, p, st);
-    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, p, st);
-    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(ta, tb, p, st);
+    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, p, st, pdl);
+    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, p, st, pdl);
+    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(ta, tb, p, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -458,10 +465,10 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
                           const int32_t* padded_offsets, int E, int64_t cap, int I, int K, const uint8_t* w2_fp4,
                           const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
                           const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
-                          int32_t* status, cudaStream_t st) {
+                          int32_t* status, cudaStream_t st, bool pdl) {
   if (use_stream_gemm(cap, E, I))
     return launch_stream_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, cap, I, K, w2_fp4, w2_sf, gs_w2,
-                                 epilogue, y_rows, slot_token, slot_weight, out32, T, status, st);
+                                 epilogue, y_rows, slot_token, slot_weight, out32, T, status, st, pdl);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, kBN)) return MOE_ERR_CUDA;
@@ -487,8 +494,8 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
   p.cap = cap;
   p.status = status;
   switch (epilogue) {
-    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, p, st);
-    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, p, st);
+    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, p, st, pdl);
+    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, p, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }

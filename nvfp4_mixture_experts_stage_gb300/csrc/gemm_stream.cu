@@ -36,7 +36,11 @@ template <int CHUNK>
 struct Cfg {
   static constexpr int kStages = CHUNK == 32 ? 8 : 6;
   static constexpr int kBStage = CHUNK * 128;            // CHUNK slot rows x 256 fp4
-  static constexpr int kSfbBase = 2 * CHUNK;             // two accumulators of CHUNK columns first
+  // Accumulators first: one per issuer, double-buffered when they fit (32-slot chunks
+  // fill the 512 columns exactly), so the issuers start a tile while the epilogue is
+  // still reading the previous one.
+  static constexpr int kAccBufs = CHUNK == 32 ? 2 : 1;
+  static constexpr int kSfbBase = 2 * CHUNK * kAccBufs;
   static constexpr int kSfwBase = kSfbBase + 4 * 64;     // resident activation scales: 4 columns per k-step
   static constexpr uint32_t kIdesc =
       (1u << 7) | (1u << 10) | ((uint32_t)(CHUNK >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
@@ -77,6 +81,7 @@ struct Params {
   int out_cols;
   int64_t cap;
   int32_t* status;
+  int early_weights;                // request weights before griddep_wait (see the producer)
 };
 
 template <int CHUNK>
@@ -90,12 +95,13 @@ struct __align__(1024) Smem {
   uint16_t xu[CHUNK][kStageLd];     //              up values
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t tfull;                   // both issuers' MMAs of a tile done (2 arrivals)
-  uint64_t tempty;                  // epilogue has the accumulators in registers (4 warps)
+  uint64_t tfull[2];                // per accumulator buffer: both issuers' MMAs of a tile done (2 arrivals)
+  uint64_t tempty[2];               // per buffer: epilogue has the accumulators in registers (4 warps)
   uint64_t drain[2];                // issuer r's MMAs so far done (one arrival per chunk switch)
   uint64_t fin[2];
   uint64_t img_full;
   uint64_t img_free;
+  uint64_t dep;                     // the producer's griddep_wait() has returned
   uint32_t tmem_base;
   int abort_flag;
   int bad_offsets;
@@ -130,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kChunk = CHUNK;
   constexpr int kStages = C::kStages;
   constexpr int kBStage = C::kBStage;
+  constexpr int kAccBufs = C::kAccBufs;
   constexpr int kSfbBase = C::kSfbBase;
   constexpr int kSfwBase = C::kSfwBase;
   constexpr uint32_t kIdesc = C::kIdesc;
@@ -141,8 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) s.bad_offsets = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.poff[i] = p.padded_offsets[i];
-  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s.cnt[i] = p.offsets[i + 1] - p.offsets[i];
+  // The routing tables were written before the previous kernel of the layer started
+  // (see the producer below), so they are read before griddep_wait(), from L2.
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.poff[i] = __ldcg(p.padded_offsets + i);
+  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s.cnt[i] = __ldcg(p.offsets + i + 1) - __ldcg(p.offsets + i);
   __syncthreads();
   for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
     const int lo = s.poff[i], hi = s.poff[i + 1], c = s.cnt[i];
@@ -170,14 +179,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
     }
-    mbar_init(&s.tfull, 2);
-    mbar_init(&s.tempty, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 2);
+      mbar_init(&s.tempty[i], 4);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.drain[i], 1);
       mbar_init(&s.fin[i], 1);
     }
     mbar_init(&s.img_full, 1);
     mbar_init(&s.img_free, 2);
+    mbar_init(&s.dep, 1);
     s.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -191,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
   const uint32_t tmem = s.tmem_base;
 
   const bool bad = s.bad_offsets != 0;
@@ -204,6 +217,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Under programmatic dependent launch this kernel may start while the previous
+    // kernel of the layer is still running.  Only the operand B rows (activations)
+    // and their scales come from that kernel.  With early_weights the first ring's
+    // worth of weight tiles is requested before griddep_wait(), and their B tiles
+    // right after it; the tile walk itself depends on the routing tables, which are
+    // complete by then (moe_forward launches this kernel only behind a kernel that
+    // waited for them).  L2 does this (it overlaps the tail of L1, which is also
+    // streaming weights); L1 does not, since the quantiser before it is a chain of
+    // short dependent memory round trips that queueing behind a burst of weight
+    // requests would slow down several-fold.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -211,6 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[kStages];
       for (int i = 0; i < kStages; ++i) issued[i] = false;
       bool ok = true;
+      // the first n_pre k-blocks: weights now, B rows once the previous kernel is done
+      const int n_pre = p.early_weights ? min(kStages, (t_hi - t_lo) * nkb) : 0;
+      int pre_row[kStages];
+      int j = 0;  // k-blocks issued
+      bool waited = false;
+      // One thread per CTA waits for the previous grid; the builder waits on s.dep.
+      if (n_pre == 0) {
+        griddep_wait();
+        mbar_arrive(&s.dep);
+        waited = true;
+      }
+      auto wait_then_issue_pre_b = [&]() {
+        griddep_wait();
+        mbar_arrive(&s.dep);
+        waited = true;
+        for (int i = 0; i < j; ++i) tma_load_2d(s.b[i], &tmap_x, &s.full[i], (i % nkb) * 128, pre_row[i]);
+      };
       Cursor<CHUNK> cur;
       for (int t = t_lo; t < t_hi && ok; ++t) {
         int c, n;
@@ -218,25 +258,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e = cur.e;
         const int row_x = s.poff[e] + c * kChunk;
         const uint8_t* sfw_src = p.w_sf + ((int64_t)e * (p.w_rows >> 7) + n) * (int64_t)ksf4 * 512;
+        const int yw = kL1 ? e * p.w_rows + n * 64 : e * p.w_rows + n * 128;
         for (int kb = 0; kb < nkb; ++kb) {
           const int natoms = min(4, ksf4 - 4 * kb);
           if (!wait_bar_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.full[stage], kWStage + kBStage + natoms * 512);
           const int x = kb * 128;
-          if (kL1) {
-            const int yw = e * p.w_rows + n * 64;
-            tma_load_2d(s.w[stage], &tmap_w, &s.full[stage], x, yw);
-            tma_load_2d(s.w[stage] + kWStage / 2, &tmap_w, &s.full[stage], x, yw + p.I);
-          } else {
-            tma_load_2d(s.w[stage], &tmap_w, &s.full[stage], x, e * p.w_rows + n * 128);
-          }
-          tma_load_2d(s.b[stage], &tmap_x, &s.full[stage], x, row_x);
+          tma_load_2d(s.w[stage], &tmap_w, &s.full[stage], x, yw);
+          if (kL1) tma_load_2d(s.w[stage] + kWStage / 2, &tmap_w, &s.full[stage], x, yw + p.I);
+          if (waited)
+            tma_load_2d(s.b[stage], &tmap_x, &s.full[stage], x, row_x);
+          else
+            pre_row[j] = row_x;
           bulk_load(s.sfw[stage], sfw_src + kb * 4 * 512, natoms * 512, &s.full[stage]);
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++j == n_pre) wait_then_issue_pre_b();
         }
       }
+      if (!waited) wait_then_issue_pre_b();  // no k-blocks, or stopped early
       if (!ok || *(volatile int*)abort_flag)
         for (int i = 0; i < kStages; ++i)
           if (issued[i]) wait_bar_drain(&s.full[i], issued_phase[i]);
@@ -253,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int it = 0, ch = -1, last_e = -1, last_c = -1;
       uint32_t g = 0;  // k-blocks of earlier tiles (ring position)
+      // shared-memory descriptors of stage 0 / image 0; others are fixed offsets (the
+      // start-address field holds address/16 and every address here is below 256 KB)
+      const uint64_t dw0 = sdesc_sw128(s.w[0]), db0 = sdesc_sw128(s.b[0]);
+      const uint64_t dsf0 = sdesc_sf(s.sfw[0]), dimg0 = sdesc_sf(s.img[0]);
       Cursor<CHUNK> cur;
       for (int t = t_lo; t < t_hi && ok; ++t, ++it, g += nkb) {
         int c, n;
@@ -272,9 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bar_bounded(&s.img_full, ch & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
         }
-        if (!wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        const int buf = it % kAccBufs;
+        const uint32_t use = (uint32_t)(it / kAccBufs);  // earlier tiles in this buffer
+        if (!wait_bar_bounded(&s.tempty[buf], (use & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + r * kChunk;
+        const uint32_t d = tmem + (2 * buf + r) * kChunk;
         bool first = true;
         for (int kb = r; kb < nkb; kb += 2) {
           const uint32_t gs = g + kb;
@@ -284,25 +331,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bar_bounded(&s.full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sfw_col = tmem + kSfwBase + 16 * stage;
-          for (int a = 0; a < natoms; ++a) tc_cp_sf(sfw_col + 4 * a, sdesc_sf(s.sfw[stage] + 512 * a));
-          if (fresh)
-            for (int a = 0; a < natoms; ++a)
-              tc_cp_sf(tmem + kSfbBase + 4 * (4 * kb + a), sdesc_sf(s.img[4 * kb + a]));
-          for (int kk = 0; kk < natoms; ++kk)
-            tc_mma_fp4(d, sdesc_sw128(s.w[stage] + 32 * kk), sdesc_sw128(s.b[stage] + 32 * kk), kIdesc,
-                       sfw_col + 4 * kk, tmem + kSfbBase + 4 * (4 * kb + kk), (!first || kk > 0) ? 1u : 0u);
+          const uint32_t sfb_col = tmem + kSfbBase + 16 * kb;
+          const uint64_t dsf = dsf0 + (uint64_t)(stage * (kSfwStage >> 4));
+          const uint64_t dw = dw0 + (uint64_t)(stage * (kWStage >> 4));
+          const uint64_t db = db0 + (uint64_t)(stage * (kBStage >> 4));
+          const uint64_t dimg = dimg0 + (uint64_t)(kb * (4 * 512 >> 4));
+          if (natoms == 4) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) tc_cp_sf(sfw_col + 4 * a, dsf + 32 * a);
+            if (fresh) {
+#pragma unroll
+              for (int a = 0; a < 4; ++a) tc_cp_sf(sfb_col + 4 * a, dimg + 32 * a);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_fp4(d, dw + 2 * kk, db + 2 * kk, kIdesc, sfw_col + 4 * kk, sfb_col + 4 * kk,
+                         (!first || kk > 0) ? 1u : 0u);
+          } else {
+            for (int a = 0; a < natoms; ++a) tc_cp_sf(sfw_col + 4 * a, dsf + 32 * a);
+            if (fresh)
+              for (int a = 0; a < natoms; ++a) tc_cp_sf(sfb_col + 4 * a, dimg + 32 * a);
+            for (int kk = 0; kk < natoms; ++kk)
+              tc_mma_fp4(d, dw + 2 * kk, db + 2 * kk, kIdesc, sfw_col + 4 * kk, sfb_col + 4 * kk,
+                         (!first || kk > 0) ? 1u : 0u);
+          }
           tc_commit(&s.empty[stage]);
           first = false;
         }
         if (!ok) break;
         if (fresh) tc_commit(&s.img_free);  // images may be rebuilt once both issuers' copies are done
-        tc_commit(&s.tfull);  // arrives once this issuer's MMAs of the tile are done
+        tc_commit(&s.tfull[buf]);  // arrives once this issuer's MMAs of the tile are done
       }
       tc_commit(&s.fin[r]);
       wait_bar_drain(&s.fin[r], 0);
     }
   } else if (warp == 6) {
     // ------------------------------------------------------------ activation-scale images
+    wait_bar_bounded(&s.dep, 0, abort_flag, p.status);  // the scales come from the previous kernel
+    // Image row i (16 B) of k-step k: bytes 0..3 the scales of chunk row i, bytes 4..7
+    // those of row 32+i (64-slot chunks), the rest zero.  The zeros are written once;
+    // every chunk then gathers its 4-byte words with asynchronous copies, all in
+    // flight at once (one memory round trip per chunk, not one per k-step batch).
+    for (int k = 0; k < ksf4; ++k) *reinterpret_cast<uint4*>(&s.img[k][lane * 16]) = make_uint4(0u, 0u, 0u, 0u);
     int ch = -1, last_e = -1, last_c = -1;
     Cursor<CHUNK> cur;
     for (int t = t_lo; t < t_hi; ++t) {
@@ -313,30 +383,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_e = cur.e;
       last_c = c;
       if (!wait_bar_bounded(&s.img_free, (ch & 1) ^ 1, abort_flag, p.status)) break;
-      // image row i (16 B): scales of chunk rows i and 32+i for k-step k, then zeros
       const int64_t r0 = (int64_t)s.poff[cur.e] + c * kChunk + lane;
-      const int64_t r1 = kChunk == 64 ? r0 + 32 : r0;  // (a 32-slot chunk uses byte group 0 only)
       const uint8_t* base0 = p.a_sf + (r0 >> 7) * (int64_t)ksf4 * 512 + (r0 & 31) * 16 + ((r0 >> 5) & 3) * 4;
-      const uint8_t* base1 = p.a_sf + (r1 >> 7) * (int64_t)ksf4 * 512 + (r1 & 31) * 16 + ((r1 >> 5) & 3) * 4;
-      for (int k0 = 0; k0 < ksf4; k0 += 8) {
-        uint32_t s0[8], s1[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (k0 + j < ksf4) {
-            s0[j] = __ldg(reinterpret_cast<const uint32_t*>(base0 + (k0 + j) * 512));
-            s1[j] = __ldg(reinterpret_cast<const uint32_t*>(base1 + (k0 + j) * 512));
-          }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (k0 + j < ksf4)
-            *reinterpret_cast<uint4*>(&s.img[k0 + j][lane * 16]) = make_uint4(s0[j], kChunk == 64 ? s1[j] : 0u, 0u, 0u);
+      for (int k = 0; k < ksf4; ++k) cp_async4(&s.img[k][lane * 16], base0 + k * 512);
+      if (kChunk == 64) {
+        const int64_t r1 = r0 + 32;
+        const uint8_t* base1 = p.a_sf + (r1 >> 7) * (int64_t)ksf4 * 512 + (r1 & 31) * 16 + ((r1 >> 5) & 3) * 4;
+        for (int k = 0; k < ksf4; ++k) cp_async4(&s.img[k][lane * 16 + 4], base1 + k * 512);
       }
+      cp_async_wait_all();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.img_full);
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
+    // Everything this role reads that the previous kernel wrote (the activation
+    // global scale) is read after a tile's accumulators are complete, hence after
+    // the producer's griddep_wait(); the routing tables are older than that kernel.
     const int q = warp & 3;           // TMEM lane quarter = weight rows 32q..32q+31
     const int tid = threadIdx.x - 64; // 0..127 over the four epilogue warps
     int it = 0;
@@ -346,11 +410,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c, n;
       cur.locate(s, p.n_tiles, t, c, n);
       const int e = cur.e;
-      wait_bar_bounded(&s.tfull, it & 1, abort_flag, p.status);
+      const int cnt_c = min(kChunk, s.cnt[e] - c * kChunk);  // valid slots of this chunk
+      const int64_t row0 = (int64_t)s.poff[e] + c * kChunk;
+      // per-slot scatter targets, fetched while the MMAs run: lane i holds slot i (+32)
+      int32_t tok_l[kChunk / 32];
+      float w_l[kChunk / 32];
+      if (KIND == kL2Scatter) {
+#pragma unroll
+        for (int h = 0; h < kChunk / 32; ++h) {
+          const bool v = 32 * h + lane < cnt_c;
+          tok_l[h] = v ? __ldg(p.slot_token + row0 + 32 * h + lane) : -1;
+          w_l[h] = v ? __ldg(p.slot_weight + row0 + 32 * h + lane) : 0.0f;
+        }
+      }
+      const int buf = it % kAccBufs;
+      wait_bar_bounded(&s.tfull[buf], (uint32_t)(it / kAccBufs) & 1, abort_flag, p.status);
       epi_bar();  // every epilogue warp has arrived (and sees an abort set before)
       if (*(volatile int*)abort_flag) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + 2 * buf * kChunk;
       float v[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; j += 16) tmem_ld16(taddr + j, *reinterpret_cast<float(*)[16]>(&v[j]));
@@ -365,10 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.tempty);  // accumulators free: values are in registers
+      if (lane == 0) mbar_arrive(&s.tempty[buf]);  // accumulators free: values are in registers
 
-      const int cnt_c = min(kChunk, s.cnt[e] - c * kChunk);  // valid slots of this chunk
-      const int64_t row0 = (int64_t)s.poff[e] + c * kChunk;
       if (kL1) {
         const float gs_a = __ldg(p.gs_a);
         const bool up = q >= 2;
@@ -459,17 +535,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col = n * 128 + q * 32 + lane;  // output column
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          if (j < cnt_c) {
+          if (j < cnt_c) {  // uniform across the warp
             const float y = round_bf16(__fmul_rn(alpha, v[j]));
             const int64_t prow = row0 + j;
             if (KIND == kL2Rows) {
               reinterpret_cast<__nv_bfloat16*>(p.out_bf16)[prow * p.out_ld + col] = __float2bfloat16_rn(y);
             } else {
-              const int32_t tok = __ldg(p.slot_token + prow);
+              const int32_t tok = __shfl_sync(0xFFFFFFFFu, tok_l[j >> 5], j & 31);
+              const float wt = __shfl_sync(0xFFFFFFFFu, w_l[j >> 5], j & 31);
               if (tok >= p.T) {
                 set_status(p.status, MOE_ERR_DEVICE_INDEX);
               } else if (tok >= 0) {
-                atomicAdd(p.out32 + (int64_t)tok * p.out_cols + col, __fmul_rn(__ldg(p.slot_weight + prow), y));
+                atomicAdd(p.out32 + (int64_t)tok * p.out_cols + col, __fmul_rn(wt, y));
               }
             }
           }
@@ -491,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int KIND, int CHUNK>
-static moe_status launch_chunk(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, cudaStream_t st) {
+static moe_status launch_chunk(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, cudaStream_t st,
+                               bool pdl) {
   constexpr size_t kSmemBytes = sizeof(Smem<CHUNK>) + 1024;
   static bool configured = false;
   if (!configured) {
@@ -500,14 +578,16 @@ static moe_status launch_chunk(const CUtensorMap& tw, const CUtensorMap& tx, con
       return MOE_ERR_CUDA;
     configured = true;
   }
-  stream_gemm_kernel<KIND, CHUNK><<<num_sms(), kThreads, kSmemBytes, st>>>(tw, tx, p);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_ex(stream_gemm_kernel<KIND, CHUNK>, num_sms(), kThreads, kSmemBytes, st, pdl, tw, tx, p) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 template <int KIND>
 static moe_status launch_kind(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, int chunk,
-                              cudaStream_t st) {
-  return chunk == 32 ? launch_chunk<KIND, 32>(tw, tx, p, st) : launch_chunk<KIND, 64>(tw, tx, p, st);
+                              cudaStream_t st, bool pdl) {
+  return chunk == 32 ? launch_chunk<KIND, 32>(tw, tx, p, st, pdl) : launch_chunk<KIND, 64>(tw, tx, p, st, pdl);
 }
 
 }  // namespace stream
@@ -518,7 +598,7 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
                                  const int32_t* padded_offsets, int E, int64_t cap, int K, int I,
                                  const uint8_t* w1_fp4, const uint8_t* w1_sf, const float* gs_g, const float* gs_u,
                                  int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4, uint8_t* h_sf,
-                                 const float* gs_h, int32_t* status, cudaStream_t st) {
+                                 const float* gs_h, int32_t* status, cudaStream_t st, bool pdl) {
   using namespace stream;
   const int chunk = stream_chunk(cap, E);
   CUtensorMap tw, tx;
@@ -545,12 +625,14 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
   p.gs_h = gs_h;
   p.cap = cap;
   p.status = status;
-  if (epilogue == MOE_L1_SILU_BF16 && h_amax && cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (epilogue == MOE_L1_SILU_BF16 && h_amax) {
+    if (cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
+    pdl = false;  // the predecessor is now the memset, not a kernel
+  }
   switch (epilogue) {
-    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(tw, tx, p, chunk, st);
-    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(tw, tx, p, chunk, st);
-    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(tw, tx, p, chunk, st);
+    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(tw, tx, p, chunk, st, pdl);
+    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(tw, tx, p, chunk, st, pdl);
+    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(tw, tx, p, chunk, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -559,7 +641,7 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
                                  const int32_t* padded_offsets, int E, int64_t cap, int I, int K,
                                  const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2, int epilogue,
                                  void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
-                                 int64_t T, int32_t* status, cudaStream_t st) {
+                                 int64_t T, int32_t* status, cudaStream_t st, bool pdl) {
   using namespace stream;
   const int chunk = stream_chunk(cap, E);
   CUtensorMap tw, tx;
@@ -572,6 +654,7 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
   p.padded_offsets = padded_offsets;
   p.E = E;
   p.Kred = I;
+  p.early_weights = 1;
   p.n_tiles = K / 128;
   p.w_rows = K;
   p.I = I;
@@ -587,8 +670,8 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
   p.cap = cap;
   p.status = status;
   switch (epilogue) {
-    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(tw, tx, p, chunk, st);
-    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(tw, tx, p, chunk, st);
+    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(tw, tx, p, chunk, st, pdl);
+    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(tw, tx, p, chunk, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }

@@ -35,8 +35,10 @@ struct QuantArgs {
 // Host launchers (each translation unit launches its own kernels).
 cudaError_t launch_amax(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, int blocks,
                         cudaStream_t st);
-cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st);
-cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st);
+// pdl: launched as a programmatic dependent of the previous kernel in the stream
+// (only where that kernel and everything before it is known; see moe_forward).
+cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st, bool pdl = false);
+cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st, bool pdl = false);
 cudaError_t launch_prepare_weight_sf(const uint8_t* src, uint8_t* dst, int E, int N, int k_sf, int gateup,
                                      int blocks, cudaStream_t st);
 
@@ -81,12 +83,12 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
                           const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
                           const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
                           float* h_amax, uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h, int32_t* status,
-                          cudaStream_t st);
+                          cudaStream_t st, bool pdl = false);
 moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
                           const int32_t* padded_offsets, int E, int64_t cap, int I, int K, const uint8_t* w2_fp4,
                           const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
                           const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
-                          int32_t* status, cudaStream_t st);
+                          int32_t* status, cudaStream_t st, bool pdl = false);
 
 // ---- gemm_stream.cu (weight-streaming kernel for small per-expert slot counts) ----
 bool stream_gemm_supported(int Kred);
@@ -94,12 +96,12 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
                                  const int32_t* padded_offsets, int E, int64_t cap, int K, int I,
                                  const uint8_t* w1_fp4, const uint8_t* w1_sf, const float* gs_g, const float* gs_u,
                                  int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4, uint8_t* h_sf,
-                                 const float* gs_h, int32_t* status, cudaStream_t st);
+                                 const float* gs_h, int32_t* status, cudaStream_t st, bool pdl = false);
 moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
                                  const int32_t* padded_offsets, int E, int64_t cap, int I, int K,
                                  const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2, int epilogue,
                                  void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
-                                 int64_t T, int32_t* status, cudaStream_t st);
+                                 int64_t T, int32_t* status, cudaStream_t st, bool pdl = false);
 
 // Which grouped-GEMM kernel runs (process-wide; moe_set_gemm_policy).
 int gemm_policy();

@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint4* __restrict_
 // ---------------------------------------------------------------------------
 template <int DST>
 __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
+  griddep_wait();  // everything read below comes from earlier kernels
+  griddep_launch_dependents();
   float amax_f = 0.0f;
   if (!a.gs_fixed) {
     if (a.amax_partials) {  // reduce the per-block maxima (non-negative: bits order like values)
@@ -173,14 +175,13 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
   }
 }
 
-cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st) {
+cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st, bool pdl) {
   switch (dst) {
-    case kDstRowMajorSf: quantize_kernel<kDstRowMajorSf><<<blocks, 256, 0, st>>>(a); break;
-    case kDstSwizzledSf: quantize_kernel<kDstSwizzledSf><<<blocks, 256, 0, st>>>(a); break;
-    case kDstSlots: quantize_kernel<kDstSlots><<<blocks, 256, 0, st>>>(a); break;
-    default: quantize_kernel<kDstMasked><<<blocks, 256, 0, st>>>(a); break;
+    case kDstRowMajorSf: return launch_ex(quantize_kernel<kDstRowMajorSf>, blocks, 256, 0, st, pdl, a);
+    case kDstSwizzledSf: return launch_ex(quantize_kernel<kDstSwizzledSf>, blocks, 256, 0, st, pdl, a);
+    case kDstSlots: return launch_ex(quantize_kernel<kDstSlots>, blocks, 256, 0, st, pdl, a);
+    default: return launch_ex(quantize_kernel<kDstMasked>, blocks, 256, 0, st, pdl, a);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_amax(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, int blocks,
@@ -194,6 +195,7 @@ cudaError_t launch_amax(const void* x, int64_t rows, int K, int64_t ld_x, uint32
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) cast_f32_bf16_kernel(const float4* __restrict__ in,
                                                             uint4* __restrict__ out, int64_t n8) {
+  griddep_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const float4 a = __ldcs(in + 2 * i), b = __ldcs(in + 2 * i + 1);
@@ -233,10 +235,9 @@ __global__ void prepare_weight_sf_kernel(const uint8_t* __restrict__ src, uint8_
   }
 }
 
-cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st) {
-  cast_f32_bf16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(in), reinterpret_cast<uint4*>(out),
-                                              n8);
-  return cudaGetLastError();
+cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st, bool pdl) {
+  return launch_ex(cast_f32_bf16_kernel, blocks, 256, 0, st, pdl, reinterpret_cast<const float4*>(in),
+                   reinterpret_cast<uint4*>(out), n8);
 }
 
 cudaError_t launch_prepare_weight_sf(const uint8_t* src, uint8_t* dst, int E, int N, int k_sf, int gateup,

@@ -46,6 +46,11 @@ MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// 4-byte global -> shared copy that completes asynchronously (cp_async_wait_all).
+MOE_DEV void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+MOE_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 MOE_DEV void tc_commit(uint64_t* bar) {
