@@ -1,4 +1,5 @@
-// Persistent grouped NVFP4 x NVFP4 GEMM on tcgen05 block-scaled MMA (sm_103a).
+// Persistent grouped NVFP4 x NVFP4 GEMM on tcgen05 block-scaled MMA (sm_103a), for
+// experts that own many slots (prefill): the tensor-bound case.
 //
 // Method: nvfp4-megamoe-kernel commits of src/nvfp4_megamoe_kernel/nvfp4_mega_moe.py
 // ("global scale as alpha": D = alpha * A @ B per expert, alpha = product of the
@@ -7,35 +8,50 @@
 // ("intermediate_size": gate | up split at I; int32 expert offsets) and of tests
 // ("complete pipeline": SiLU(gate)*up in BF16, requantise, weighted scatter).
 //
-// Structure (one CTA per SM, 6 warps):
-//   warp 0      TMA producer: A tile (128 slot rows x 128 B = 256 fp4 of K), B tile
-//               (128 weight rows; for L1 64 gate rows + the matching 64 up rows),
-//               and the 4 scale atoms of each operand for the same K range, into a
-//               6-stage shared-memory ring guarded by full/empty mbarriers.
-//   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp moves the scale
-//               atoms into TMEM (32x128b, replicated to the 4 lane quarters), then
-//               four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128,
-//               N=128, K=64) accumulate fp32 into one of two TMEM accumulators.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows (one row per thread),
-//               alpha, BF16 rounding, and the fused per-layer tail (SiLU*up and
-//               requantisation for L1, weighted fp32 scatter-add for L2), while the
-//               MMA warp fills the other accumulator.
-// Tiles are (expert, n-tile, m-tile) with the m-tiles of one weight block adjacent,
-// so CTAs running at the same time share weight tiles through L2; the expert of a
-// tile comes from the padded offsets on the device (no host sync).
+// Tile: 128 slot rows (M) x BN weight rows (N = 256, or 128 where the shape needs
+// it), K staged 256 elements at a time.  For L1 a 256-row tile is two prepared
+// 128-row blocks, each 64 gate rows then the matching 64 up rows (128 h columns).
+// One CTA per SM, 12 warps:
+//   warp 0      TMA producer: A (slot rows), B (weight rows) and their scale atoms
+//               into a shared-memory ring (full/empty mbarriers).
+//   warp 1      MMA issuer and TMEM owner: only tcgen05.mma (M=128, N=BN, K=64),
+//               four per stage, into one TMEM accumulator of BN columns.
+//   warps 2, 3  scale copiers: tcgen05.cp of the stage's scale atoms into TMEM (each
+//               warp two of the four k-steps), then a commit that releases the stage
+//               to the MMA warp.  Issued from other warps than the MMAs: one thread
+//               issuing both spends about twice as long per stage (measured).
+//   warps 4-11  epilogue: two warps per TMEM lane quarter, each taking half of the
+//               accumulator columns into registers; the accumulator is released as
+//               soon as all eight have loaded, before the epilogue math, so the next
+//               tile's MMAs wait only for the TMEM reads.
+// Tiles are (expert, n-tile, m-tile), m fastest, dealt round-robin over the CTAs, so
+// CTAs running at the same time share weight tiles through L2; the expert of a tile
+// comes from the padded offsets on the device (no host sync).
 #include "tcgen05.cuh"
 
 namespace moe {
 
-constexpr int kBM = 128, kBN = 128;
+constexpr int kBM = 128;
 constexpr int kBKBytes = 128;               // 256 fp4 per row per stage
-constexpr int kStages = 6;
-constexpr int kAStage = kBM * kBKBytes;     // 16 KB
-constexpr int kBStage = kBN * kBKBytes;     // 16 KB
-constexpr int kSfStage = 4 * 512;           // 4 scale atoms
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 384;
+constexpr int kEpiWarps = 8;
 constexpr int kTmemCols = 512;
-constexpr int kSfTmemBase = 256;            // stage s scales at 256 + 32 s (A: +0, B: +16)
+
+template <int BN>
+struct TiledCfg {
+  static constexpr int kBlocks = BN / 128;                  // 128-row weight blocks per tile
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kAStage = kBM * kBKBytes;            // 16 KB
+  static constexpr int kBStage = BN * kBKBytes;             // 32 / 16 KB
+  static constexpr int kSfaStage = 4 * 512;
+  static constexpr int kSfbStage = kBlocks * 4 * 512;
+  static constexpr int kSfbPerStep = 4 * kBlocks;           // TMEM columns of B scales per k-step
+  static constexpr int kSfCols = 16 + 4 * kSfbPerStep;      // TMEM columns of one stage's scales
+  static constexpr int kSfBase = BN;                        // accumulator first
+  static constexpr uint32_t kIdesc =
+      (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+  static_assert(kSfBase + kStages * kSfCols <= kTmemCols, "tensor memory budget");
+};
 
 enum GemmKind : int { kL1GateUp = 0, kL1Silu = 1, kL1Requant = 2, kL2Rows = 3, kL2Scatter = 4 };
 
@@ -67,15 +83,18 @@ struct GemmParams {
   int32_t* status;
 };
 
+template <int BN>
 struct __align__(1024) GemmSmem {
-  uint8_t a[kStages][kAStage];
-  uint8_t b[kStages][kBStage];
-  uint8_t sfa[kStages][kSfStage];
-  uint8_t sfb[kStages][kSfStage];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  using C = TiledCfg<BN>;
+  uint8_t a[C::kStages][C::kAStage];
+  uint8_t b[C::kStages][C::kBStage];
+  uint8_t sfa[C::kStages][C::kSfaStage];
+  uint8_t sfb[C::kStages][C::kSfbStage];
+  uint64_t full[C::kStages];
+  uint64_t empty[C::kStages];
+  uint64_t sf_ready[C::kStages];    // both copiers' scale copies of the stage done
+  uint64_t tfull;
+  uint64_t tempty;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -84,17 +103,11 @@ struct __align__(1024) GemmSmem {
   int cnt[256];
 };
 
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-
-// Bounded wait through the CTA's abort flag.
-MOE_DEV bool wait_bar(uint64_t* bar, uint32_t parity, GemmSmem& s, int32_t* status) {
-  return wait_bar_bounded(bar, parity, &s.abort_flag, status);
-}
-
 // Tile t -> (expert, n-tile, m-tile); e advances monotonically with t.
 struct TileCursor {
   int e = 0;
-  MOE_DEV bool locate(const GemmSmem& s, int E, int n_tiles, int t, int& n, int& m) {
+  template <class S>
+  MOE_DEV bool locate(const S& s, int E, int n_tiles, int t, int& n, int& m) {
     while (e < E && t >= (s.poff[e + 1] >> 7) * n_tiles) ++e;
     if (e >= E) return false;
     const int tl = t - (s.poff[e] >> 7) * n_tiles;
@@ -105,14 +118,18 @@ struct TileCursor {
   }
 };
 
-template <int KIND>
+template <int KIND, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const GemmParams p) {
+  using C = TiledCfg<BN>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
-  GemmSmem& s = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GemmSmem<BN>& s =
+      *reinterpret_cast<GemmSmem<BN>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool kL1 = KIND <= kL1Requant;
+  int* abort_flag = &s.abort_flag;
 
   griddep_wait();
   griddep_launch_dependents();
@@ -132,11 +149,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
+      mbar_init(&s.sf_ready[i], 2);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);
-    }
+    mbar_init(&s.tfull, 1);
+    mbar_init(&s.tempty, kEpiWarps);
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -175,36 +191,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int e = cur.e;
         const int row_a = s.poff[e] + m * kBM;
         const uint8_t* sfa_src = p.a_sf + ((int64_t)(row_a >> 7) * ksf4) * 512;
+        // prepared weight row blocks n*kBlocks .. n*kBlocks + kBlocks - 1 of expert e
         const uint8_t* sfb_src =
-            p.b_sf + ((int64_t)e * (p.b_rows >> 7) + n) * (int64_t)ksf4 * 512;
+            p.b_sf + ((int64_t)e * (p.b_rows >> 7) + (int64_t)n * C::kBlocks) * (int64_t)ksf4 * 512;
         for (int kb = 0; kb < nkb; ++kb) {
           const int natoms = min(4, ksf4 - 4 * kb);
-          if (!wait_bar(&s.empty[stage], phase ^ 1, s, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.full[stage], kAStage + kBStage + 2 * natoms * 512);
+          if (!wait_bar_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.full[stage], C::kAStage + C::kBStage + (1 + C::kBlocks) * natoms * 512);
           const int x = kb * kBKBytes;
           tma_load_2d(s.a[stage], &tmap_a, &s.full[stage], x, row_a);
           if (kL1) {
-            const int yb = e * p.b_rows + n * 64;
-            tma_load_2d(s.b[stage], &tmap_b, &s.full[stage], x, yb);
-            tma_load_2d(s.b[stage] + kBStage / 2, &tmap_b, &s.full[stage], x, yb + p.I);
+            // block j: 64 gate rows then the matching 64 up rows (h columns n*BN/2 + 64 j ..)
+#pragma unroll
+            for (int j = 0; j < C::kBlocks; ++j) {
+              const int yb = e * p.b_rows + n * (BN / 2) + 64 * j;
+              tma_load_2d(s.b[stage] + j * 128 * kBKBytes, &tmap_b, &s.full[stage], x, yb);
+              tma_load_2d(s.b[stage] + j * 128 * kBKBytes + 64 * kBKBytes, &tmap_b, &s.full[stage], x, yb + p.I);
+            }
           } else {
-            tma_load_2d(s.b[stage], &tmap_b, &s.full[stage], x, e * p.b_rows + n * kBN);
+#pragma unroll
+            for (int j = 0; j < C::kBlocks; ++j)
+              tma_load_2d(s.b[stage] + j * 128 * kBKBytes, &tmap_b, &s.full[stage], x, e * p.b_rows + n * BN + 128 * j);
           }
           bulk_load(s.sfa[stage], sfa_src + kb * 4 * 512, natoms * 512, &s.full[stage]);
-          bulk_load(s.sfb[stage], sfb_src + kb * 4 * 512, natoms * 512, &s.full[stage]);
+#pragma unroll
+          for (int j = 0; j < C::kBlocks; ++j)
+            bulk_load(s.sfb[stage] + j * 4 * 512, sfb_src + (int64_t)j * ksf4 * 512 + kb * 4 * 512, natoms * 512,
+                      &s.full[stage]);
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok || *(volatile int*)&s.abort_flag) {
+      if (!ok || *(volatile int*)abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
         for (int i = 0; i < kStages; ++i)
-          if (issued[i]) {
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&s.full[i], issued_phase[i]) && globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
-          }
+          if (issued[i]) wait_bar_drain(&s.full[i], issued_phase[i]);
       }
     }
   } else if (warp == 1) {
@@ -214,43 +236,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
+      const uint64_t da0 = sdesc_sw128(s.a[0]), db0 = sdesc_sw128(s.b[0]);
       TileCursor cur;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++it) {
         int n, m;
         if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
-        const int acc = it & 1;
-        if (!wait_bar(&s.tempty[acc], ((it >> 1) & 1) ^ 1, s, p.status)) { ok = false; break; }
+        if (!wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + acc * kBN;
         for (int kb = 0; kb < nkb; ++kb) {
           const int natoms = min(4, ksf4 - 4 * kb);
-          if (!wait_bar(&s.full[stage], phase, s, p.status)) { ok = false; break; }
+          if (!wait_bar_bounded(&s.full[stage], phase, abort_flag, p.status) ||
+              !wait_bar_bounded(&s.sf_ready[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t sf_col = tmem + kSfTmemBase + 32 * stage;
-          for (int a = 0; a < natoms; ++a) {
-            tc_cp_sf(sf_col + 4 * a, sdesc_sf(s.sfa[stage] + 512 * a));
-            tc_cp_sf(sf_col + 16 + 4 * a, sdesc_sf(s.sfb[stage] + 512 * a));
-          }
-          for (int kk = 0; kk < natoms; ++kk) {
-            tc_mma_fp4(d, sdesc_sw128(s.a[stage] + 32 * kk), sdesc_sw128(s.b[stage] + 32 * kk), kIdesc,
-                       sf_col + 4 * kk, sf_col + 16 + 4 * kk, (kb | kk) != 0);
-          }
+          const uint32_t sf = tmem + C::kSfBase + stage * C::kSfCols;
+          const uint64_t da = da0 + (uint64_t)((stage * C::kAStage) >> 4);
+          const uint64_t db = db0 + (uint64_t)((stage * C::kBStage) >> 4);
+          for (int kk = 0; kk < natoms; ++kk)
+            tc_mma_fp4(tmem, da + 2 * kk, db + 2 * kk, C::kIdesc, sf + 4 * kk, sf + 16 + C::kSfbPerStep * kk,
+                       (kb | kk) != 0);
           tc_commit(&s.empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc_commit(&s.tfull[acc]);
+        tc_commit(&s.tfull);
       }
       // all MMAs issued by this thread complete before TMEM is released
       tc_commit(&s.drain);
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&s.drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      wait_bar_drain(&s.drain, 0);
+    }
+  } else if (warp <= 3) {
+    // ------------------------------------------------------------ scale copiers
+    // copier c copies k-steps 2c, 2c+1 of every stage: the A atom and the kBlocks B
+    // atoms of each (B atom j of k-step kk at column 16 + kSfbPerStep*kk + 4j).
+    if (lane == 0) {
+      const int c = warp - 2;
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint64_t dsa0 = sdesc_sf(s.sfa[0]), dsb0 = sdesc_sf(s.sfb[0]);
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int natoms = min(4, ksf4 - 4 * kb);
+          if (!wait_bar_bounded(&s.full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sf = tmem + C::kSfBase + stage * C::kSfCols;
+          const uint64_t dsa = dsa0 + (uint64_t)((stage * C::kSfaStage) >> 4);
+          const uint64_t dsb = dsb0 + (uint64_t)((stage * C::kSfbStage) >> 4);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int kk = 2 * c + h;
+            if (kk < natoms) {
+              tc_cp_sf(sf + 4 * kk, dsa + 32 * kk);
+#pragma unroll
+              for (int j = 0; j < C::kBlocks; ++j)
+                tc_cp_sf(sf + 16 + C::kSfbPerStep * kk + 4 * j, dsb + 128 * j + 32 * kk);
+            }
+          }
+          tc_commit(&s.sf_ready[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int half = (warp - 4) >> 2;          // which half of the accumulator columns
     const int row = q * 32 + lane;
+    constexpr int kCols = BN / 2;              // accumulator columns per epilogue warp
     int it = 0;
     TileCursor cur;
     float amax = 0.0f;
@@ -258,30 +314,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int n, m;
       if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
       const int e = cur.e;
-      const int acc = it & 1;
-      if (!wait_bar(&s.tfull[acc], (it >> 1) & 1, s, p.status)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * kBN;
       const bool valid = m * kBM + row < s.cnt[e];
       const int64_t prow = (int64_t)s.poff[e] + m * kBM + row;
+      if (!wait_bar_bounded(&s.tfull, it & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+      // L1: columns of this warp's gate values and of the matching up values; L2: kCols
+      // consecutive output columns
+      float v[kCols];
+      if constexpr (kL1) {
+        // BN 256: half h = prepared block h (gate at 128h, up at 128h + 64), 64 columns each;
+        // BN 128: half h = gate columns 32h.., up columns 64 + 32h..
+        constexpr int G = kCols / 2;
+        const uint32_t g0 = BN == 256 ? 128 * half : 32 * half;
+        if constexpr (G == 64) {
+          tmem_ld64(taddr + g0, *reinterpret_cast<float(*)[64]>(&v[0]));
+          tmem_ld64(taddr + g0 + 64, *reinterpret_cast<float(*)[64]>(&v[G]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < G; j += 16) {
+            tmem_ld16(taddr + g0 + j, *reinterpret_cast<float(*)[16]>(&v[j]));
+            tmem_ld16(taddr + g0 + 64 + j, *reinterpret_cast<float(*)[16]>(&v[G + j]));
+          }
+        }
+      } else {
+        if constexpr (kCols % 64 == 0) {
+#pragma unroll
+          for (int j = 0; j < kCols; j += 64)
+            tmem_ld64(taddr + half * kCols + j, *reinterpret_cast<float(*)[64]>(&v[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < kCols; j += 16)
+            tmem_ld16(taddr + half * kCols + j, *reinterpret_cast<float(*)[16]>(&v[j]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.tempty);  // accumulator free: values are in registers
+
       if (kL1) {
+        constexpr int G = kCols / 2;           // h columns of this warp
+        const int hcol0 = n * (BN / 2) + (BN == 256 ? 64 * half : 32 * half);
         const float gs_a = __ldg(p.gs_a);
         const float ag = __fmul_rn(gs_a, __ldg(p.gs_b0 + e));
         const float au = __fmul_rn(gs_a, __ldg(p.gs_b1 + e));
         float rg = 0.0f;
         if (KIND == kL1Requant) rg = recip_global_scale(__ldg(p.gs_h));
         uint32_t sfw = 0;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int c = 0; c < G / 16; ++c) {
           float g[16], u[16];
-          tmem_ld16(taddr + c * 16, g);
-          tmem_ld16(taddr + 64 + c * 16, u);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            g[i] = round_bf16(__fmul_rn(ag, g[i]));
-            u[i] = round_bf16(__fmul_rn(au, u[i]));
+            g[i] = round_bf16(__fmul_rn(ag, v[16 * c + i]));
+            u[i] = round_bf16(__fmul_rn(au, v[G + 16 * c + i]));
           }
-          const int col = n * 64 + c * 16;  // h column (gate/up column) of element 0
+          const int col = hcol0 + 16 * c;  // h column (gate/up column) of element 0
           if (KIND == kL1GateUp) {
             if (valid) {
               uint4* dg = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
@@ -326,8 +414,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
-        if (KIND == kL1Requant && valid)
-          *reinterpret_cast<uint32_t*>(p.h_sf + sf_swizzle_offset(prow, n * 4, p.I >> 4)) = sfw;
+        if (KIND == kL1Requant && valid) {
+          // G/16 consecutive scale columns starting at a multiple of 2 (BN 128) or 4 (BN 256)
+          uint8_t* sp = p.h_sf + sf_swizzle_offset(prow, hcol0 >> 4, p.I >> 4);
+          if constexpr (G == 64)
+            *reinterpret_cast<uint32_t*>(sp) = sfw;
+          else
+            *reinterpret_cast<uint16_t*>(sp) = (uint16_t)sfw;
+        }
       } else {
         const float alpha = __fmul_rn(__ldg(p.gs_a), __ldg(p.gs_b0 + e));
         int32_t tok = -1;
@@ -337,13 +431,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           wgt = __ldg(p.slot_weight + prow);
           if (tok >= p.T) { set_status(p.status, MOE_ERR_DEVICE_INDEX); tok = -1; }
         }
-#pragma unroll 1
-        for (int c = 0; c < kBN / 16; ++c) {
-          float y[16];
-          tmem_ld16(taddr + c * 16, y);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) y[i] = round_bf16(__fmul_rn(alpha, y[i]));
-          const int col = n * kBN + c * 16;
+        for (int c = 0; c < kCols / 16; ++c) {
+          float y[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = round_bf16(__fmul_rn(alpha, v[16 * c + i]));
+          const int col = n * BN + half * kCols + c * 16;
           if (KIND == kL2Rows) {
             if (valid) {
               uint4* dy = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
@@ -359,9 +452,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.tempty[acc]);
     }
     if (KIND == kL1Silu && p.h_amax) {
       // non-negative floats order like their bit patterns
@@ -378,22 +468,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-constexpr size_t kGemmSmemBytes = sizeof(GemmSmem) + 1024;
-
-template <int KIND>
-static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st,
-                              bool pdl) {
+template <int KIND, int BN>
+static moe_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st,
+                            bool pdl) {
+  constexpr size_t kSmemBytes = sizeof(GemmSmem<BN>) + 1024;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kGemmSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
       return MOE_ERR_CUDA;
     configured = true;
   }
-  return launch_ex(grouped_gemm_kernel<KIND>, num_sms(), kGemmThreads, kGemmSmemBytes, st, pdl, ta, tb, p) ==
+  return launch_ex(grouped_gemm_kernel<KIND, BN>, num_sms(), kGemmThreads, kSmemBytes, st, pdl, ta, tb, p) ==
                  cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
+}
+
+template <int KIND>
+static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int bn,
+                              cudaStream_t st, bool pdl) {
+  return bn == 256 ? launch_bn<KIND, 256>(ta, tb, p, st, pdl) : launch_bn<KIND, 128>(ta, tb, p, st, pdl);
 }
 
 static int g_policy = MOE_GEMM_AUTO;
@@ -415,7 +510,7 @@ bool use_stream_gemm(int64_t cap, int E, int Kred) {
 // take several chunks) unless the policy forces 64.
 int stream_chunk(int64_t, int) { return gemm_policy() == MOE_GEMM_STREAMING_N64 ? 64 : 32; }
 
-// L1: A = slot activations [cap, K/2]; B = W1 [E*2I, K/2]; N per tile = 64 h cols.
+// L1: A = slot activations [cap, K/2]; B = W1 [E*2I, K/2]; a tile covers BN/2 h columns.
 moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a, const int32_t* offsets,
                           const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
                           const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
@@ -427,6 +522,7 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w1_fp4, (uint64_t)K / 2, (uint64_t)E * 2 * I, 64)) return MOE_ERR_CUDA;
+  const int bn = I % 128 == 0 ? 256 : 128;
   GemmParams p{};
   p.a_sf = a_sf;
   p.b_sf = w1_sf;
@@ -434,7 +530,7 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
   p.padded_offsets = padded_offsets;
   p.E = E;
   p.Kred = K;
-  p.n_tiles = I / 64;
+  p.n_tiles = I / (bn / 2);
   p.b_rows = 2 * I;
   p.I = I;
   p.cap = cap;
@@ -453,14 +549,14 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
     pdl = false;  // the predecessor is now the memset, not a kernel
   }
   switch (epilogue) {
-    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, p, st, pdl);
-    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, p, st, pdl);
-    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(ta, tb, p, st, pdl);
+    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, p, bn, st, pdl);
+    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, p, bn, st, pdl);
+    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(ta, tb, p, bn, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }
 
-// L2: A = h codes [cap, I/2]; B = W2 [E*K, I/2]; N per tile = 128 output cols.
+// L2: A = h codes [cap, I/2]; B = W2 [E*K, I/2]; a tile covers BN output columns.
 moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
                           const int32_t* padded_offsets, int E, int64_t cap, int I, int K, const uint8_t* w2_fp4,
                           const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
@@ -471,7 +567,8 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
                                  epilogue, y_rows, slot_token, slot_weight, out32, T, status, st, pdl);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
-  if (!make_tmap(&tb, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, kBN)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tb, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, 128)) return MOE_ERR_CUDA;
+  const int bn = K % 256 == 0 ? 256 : 128;
   GemmParams p{};
   p.a_sf = h_sf;
   p.b_sf = w2_sf;
@@ -479,7 +576,7 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
   p.padded_offsets = padded_offsets;
   p.E = E;
   p.Kred = I;
-  p.n_tiles = K / kBN;
+  p.n_tiles = K / bn;
   p.b_rows = K;
   p.I = I;
   p.gs_a = gs_h;
@@ -494,8 +591,8 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
   p.cap = cap;
   p.status = status;
   switch (epilogue) {
-    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, p, st, pdl);
-    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, p, st, pdl);
+    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, p, bn, st, pdl);
+    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, p, bn, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }
