@@ -262,8 +262,9 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const 
  *                      implies at most 64 slots per local expert on average
  *                      (capacity - 127*E <= 64*E) and the contraction is <= 4096,
  *                      the tiled kernel otherwise;
- *   MOE_GEMM_TILED     always the tiled kernel: 128 slot rows x 128 weight rows per
- *                      tile, slots on the MMA's M side;
+ *   MOE_GEMM_TILED     always the tiled kernel: 128 slot rows x 256 weight rows per
+ *                      tile (128 where I % 128 or, for L2, K % 256 leaves no
+ *                      choice), slots on the MMA's M side;
  *   MOE_GEMM_STREAMING the weight-streaming kernel whenever the contraction is
  *                      <= 4096: weight rows on the MMA's M side, chunks of slots on
  *                      its N side, the chunk's activation scales resident in tensor
@@ -285,6 +286,20 @@ int moe_set_gemm_policy(int policy);
 moe_status moe_cast_output(const float* out32, void* out_bf16, int64_t T, int K,
                            moe_stream_t stream);
 
+/* Weighted combine of per-slot L2 rows (the scatter_add of the nvfp4-megamoe-kernel
+ * pages done per token instead of with atomics):
+ *   out_bf16[t, :] = bf16( sum_j w[t, j] * y_rows[pair_slot[t*topk + j], :] )
+ * over j = 0 .. topk-1 in that order, in fp32 with each product and each sum
+ * rounded (the oracle's combine bit for bit); pairs with slot -1 are skipped, so a
+ * token with no local expert gets 0.
+ *   y_rows [capacity, ld_y] BF16 (the MOE_L2_ROWS_BF16 output), ld_y >= K, ld_y % 8 == 0;
+ *   pair_slot [T*topk] from moe_route; topk_w [T, topk] fp32; out_bf16 [T, K].
+ *   K % 8 == 0; y_rows and out_bf16 16-byte aligned.  A slot >= capacity is skipped
+ *   and reported as MOE_ERR_DEVICE_INDEX in *dev_status (if not NULL). */
+moe_status moe_combine_rows(const void* y_rows, int64_t ld_y, const int32_t* pair_slot,
+                            const float* topk_w, int64_t T, int topk, int K, int64_t capacity,
+                            void* out_bf16, int32_t* dev_status, moe_stream_t stream);
+
 /* Expert weights of one rank, all device memory. */
 typedef struct moe_weights {
     const uint8_t* w1_fp4;      /* [E, 2I, K/2]                          */
@@ -298,7 +313,10 @@ typedef struct moe_weights {
 
 /* The whole rank-local layer (nvfp4_moe_full / the CuTeDSL runner's forward):
  * route -> quantise x into slots -> L1 (+SiLU*up, +requant) -> L2 (+weighted
- * scatter) -> BF16 output.  The caller sums outputs across ranks.
+ * scatter) -> BF16 output.  The caller sums outputs across ranks.  While the fp32
+ * output accumulator (T*K*4 bytes) is at most 32 MiB the weighted scatter is fused
+ * into the L2 epilogue (fp32 atomics, then a cast); above that the L2 GEMM writes
+ * BF16 rows and moe_combine_rows' arithmetic produces the output.
  *   x [T, K] BF16 (row stride K); topk_ids/topk_w [T, topk]; out [T, K] BF16.
  *   gs_x_fixed: NULL -> amax of x; else a fixed fp32 global scale.
  *   gs_h_mode MOE_GS_DYNAMIC: gs_h (device fp32) receives max|h|/2688;
@@ -317,7 +335,7 @@ moe_status moe_forward(const void* x, int64_t T, int K, int I, int E,
  * caller, with timing enabled) recorded on `stream` at: [0] start, [1] after
  * routing, [2] after quantising x into the slots, [3] after the L1 GEMM,
  * [4] after requantising h (equal to [3] in MOE_GS_FIXED mode), [5] after the
- * L2 GEMM, [6] after the output cast.  While the stream is being captured into
+ * L2 GEMM, [6] after the output cast or combine.  While the stream is being captured into
  * a CUDA graph the records become event-record nodes of the graph.  All other
  * arguments and behaviour are those of moe_forward. */
 #define MOE_TRACE_EVENTS 7

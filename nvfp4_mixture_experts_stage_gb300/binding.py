@@ -37,7 +37,7 @@ EXPORTS = (
     "moe_stage_activation", "moe_stage_activation_to_slots", "moe_route",
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
     "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
-    "moe_set_gemm_policy",
+    "moe_set_gemm_policy", "moe_combine_rows",
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
@@ -81,6 +81,7 @@ def _load():
         "moe_requant": (I32, [P, I64, I32, P, P, P, P, P, P, P]),
         "moe_grouped_gemm_l2": (I32, [P, P, P, P, P, I32, I64, I32, I32, P, P, P, I32, P, P, P, P, I64, P, P]),
         "moe_cast_output": (I32, [P, P, I64, I32, P]),
+        "moe_combine_rows": (I32, [P, I64, P, P, I64, I32, I32, I64, P, P, P]),
         "moe_set_gemm_policy": (I32, [I32]),
         "moe_forward": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32, P, P,
                               P, P, SZ, P]),
@@ -220,6 +221,16 @@ def moe_grouped_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, I, K, w2_
 def moe_cast_output(out32, out_bf16, stream=None):
     T, K = out32.shape
     _check("moe_cast_output", _lib.moe_cast_output(_p(out32), _p(out_bf16), T, K, _stream(stream)))
+
+
+def moe_combine_rows(y_rows, pair_slot, topk_w, out_bf16, capacity=None, dev_status=None, stream=None):
+    """out_bf16[t] = bf16(sum_j w[t, j] * y_rows[pair_slot[t, j]]) (include/moe_stage.h)."""
+    T, topk = topk_w.shape
+    K = out_bf16.shape[1]
+    cap = y_rows.shape[0] if capacity is None else capacity
+    _check("moe_combine_rows", _lib.moe_combine_rows(
+        _p(y_rows), y_rows.stride(0), _p(pair_slot), _p(topk_w), T, topk, K, cap, _p(out_bf16), _p(dev_status),
+        _stream(stream)))
 
 
 def make_weights(w1_fp4, w1_sf, gs_w1_gate, gs_w1_up, w2_fp4, w2_sf, gs_w2):

@@ -96,6 +96,22 @@ moe_status cast_output(const float* out32, void* out_bf16, int64_t T, int K, cud
   return launch_cast(out32, out_bf16, n8, blocks, stream, pdl) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+moe_status combine_rows(const void* y_rows, int64_t ld_y, const int32_t* pair_slot, const float* topk_w, int64_t T,
+                        int topk, int K, int64_t capacity, void* out_bf16, int32_t* dev_status, cudaStream_t stream,
+                        bool pdl) {
+  if (T < 0 || K <= 0 || K % 8 || topk < 1 || topk > 32 || ld_y < K || ld_y % 8 || capacity < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y_rows || !pair_slot || !topk_w || !out_bf16 || !aligned(y_rows, 16) || !aligned(out_bf16, 16))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t n8 = T * K / 8;
+  const int blocks = (int)std::min<int64_t>(ceil_div(n8, 256), (int64_t)sm_count() * 8);
+  return launch_combine(y_rows, ld_y, pair_slot, topk_w, topk, T, K, capacity, out_bf16, dev_status, blocks, stream,
+                        pdl) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 moe_status mark(void* const* events, int i, cudaStream_t st) {
   if (!events || !events[i]) return MOE_OK;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -145,6 +161,19 @@ size_t moe_route_workspace_size(int64_t T, int topk, int E) {
 
 size_t moe_stage_workspace_size(void) { return 256; }
 
+// Output path of moe_forward.  Small batches scatter w*y with fp32 atomics into an
+// accumulator of T*K fp32 (L2-resident) and cast it; once that accumulator outgrows
+// a quarter of L2, the atomics would thrash it through HBM (each row receives topk
+// scattered updates), so the L2 GEMM writes its BF16 rows instead and one kernel
+// combines each token's rows in pair order.
+constexpr int64_t kCombineMinOutBytes = 32ll << 20;
+static bool use_combine(int64_t T, int K) { return T * K * 4 > kCombineMinOutBytes; }
+
+// Bytes of the output region: the fp32 accumulator, or the BF16 rows of every slot.
+static int64_t out_region_bytes(int64_t T, int K, int64_t cap) {
+  return std::max<int64_t>(std::max<int64_t>(T * K * 4, 4), use_combine(T, K) ? cap * K * 2 : 0);
+}
+
 static size_t forward_layout(Carve& c, int64_t T, int K, int I, int E, int topk, void** parts) {
   const int64_t cap = moe_slot_capacity(T, topk, E);
   parts[0] = c.take<uint32_t>(512);                                  // scalars, amax partials
@@ -160,7 +189,7 @@ static size_t forward_layout(Carve& c, int64_t T, int K, int I, int E, int topk,
   parts[10] = c.take<uint16_t>(cap * I);                             // h bf16
   parts[11] = c.take<uint8_t>(cap * I / 2);                          // h codes
   parts[12] = c.take<uint8_t>(cap * I / 16);                         // h scales
-  parts[13] = c.take<float>(std::max<int64_t>(T * K, 1));            // out32
+  parts[13] = c.take<uint8_t>(out_region_bytes(T, K, cap));         // out32, or L2 rows (combine)
   return c.off;
 }
 
@@ -302,6 +331,12 @@ moe_status moe_cast_output(const float* out32, void* out_bf16, int64_t T, int K,
   return cast_output(out32, out_bf16, T, K, stream, false);
 }
 
+moe_status moe_combine_rows(const void* y_rows, int64_t ld_y, const int32_t* pair_slot, const float* topk_w, int64_t T,
+                            int topk, int K, int64_t capacity, void* out_bf16, int32_t* dev_status,
+                            moe_stream_t stream) {
+  return combine_rows(y_rows, ld_y, pair_slot, topk_w, T, topk, K, capacity, out_bf16, dev_status, stream, false);
+}
+
 moe_status moe_forward(const void* x, int64_t T, int K, int I, int E, const int32_t* topk_ids, const float* topk_w,
                        int topk, int expert_offset, const moe_weights* w, const float* gs_x_fixed, int gs_h_mode,
                        float* gs_h, void* out, int32_t* dev_status, void* ws, size_t ws_bytes,
@@ -347,6 +382,7 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
   uint8_t* h_fp4 = reinterpret_cast<uint8_t*>(parts[11]);
   uint8_t* h_sf = reinterpret_cast<uint8_t*>(parts[12]);
   float* out32 = reinterpret_cast<float*>(parts[13]);
+  const bool combine = use_combine(T, K);  // parts[13] then holds the L2 rows [cap, K] BF16
 
   moe_status s;
   // Kernels after the first run as programmatic dependents of their predecessor (each
@@ -380,8 +416,8 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     pa.vec_per_row = K / 8;
     pa.ld_vec = K / 8;
     pa.amax_partials = gs_x_fixed ? nullptr : partials;
-    pa.out32 = out32;
-    pa.out32_n4 = n4;
+    pa.out32 = combine ? nullptr : out32;
+    pa.out32_n4 = combine ? 0 : n4;
     if (launch_forward_prologue(pa, nb, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if ((s = mark(stage_events, 1, stream)) != MOE_OK) return s;
     // Not a programmatic dependent: launched early, its blocks would be placed on the
@@ -389,7 +425,8 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     s = quantize_launch(2, x, T, K, K, nullptr, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk, nullptr, cap,
                         dev_status, stream, gs_x_fixed ? nullptr : partials, nb, false);
   } else {
-    if (cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!combine && cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
     s = route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, poff, slot_token, slot_weight,
                    pair_slot, cap, rcnt, rbase, dev_status, stream);
     if (s != MOE_OK || (s = mark(stage_events, 1, stream)) != MOE_OK) return s;
@@ -415,10 +452,15 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     if (s != MOE_OK || (s = mark(stage_events, 3, stream)) != MOE_OK) return s;
   }
   if (s != MOE_OK || (s = mark(stage_events, 4, stream)) != MOE_OK) return s;
-  s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2, MOE_L2_SCATTER,
-                     nullptr, slot_token, slot_weight, out32, T, dev_status, stream, pdl);
+  if (combine)
+    s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2,
+                       MOE_L2_ROWS_BF16, parts[13], nullptr, nullptr, nullptr, T, dev_status, stream, pdl);
+  else
+    s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2, MOE_L2_SCATTER,
+                       nullptr, slot_token, slot_weight, out32, T, dev_status, stream, pdl);
   if (s != MOE_OK || (s = mark(stage_events, 5, stream)) != MOE_OK) return s;
-  s = cast_output(out32, out, T, K, stream, pdl);
+  s = combine ? combine_rows(parts[13], K, pair_slot, topk_w, T, topk, K, cap, out, dev_status, stream, pdl)
+              : cast_output(out32, out, T, K, stream, pdl);
   if (s != MOE_OK) return s;
   return mark(stage_events, 6, stream);
 }

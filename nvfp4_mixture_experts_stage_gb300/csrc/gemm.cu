@@ -38,9 +38,6 @@ constexpr int kBM = 128;
 constexpr int kBKBytes = 128;               // 256 fp4 per row per stage
 constexpr int kGemmThreads = 384;
 constexpr int kEpiWarps = 8;
-#ifndef TILED_CLUSTER
-#define TILED_CLUSTER 1
-#endif
 constexpr int kTmemCols = 512;
 
 template <int BN>
@@ -107,29 +104,25 @@ struct __align__(1024) GemmSmem {
   int bad_offsets;
   int poff[257];
   int cnt[256];
-  int cum[257];                     // work units before expert e
+  int cum[257];                     // tiles before expert e
 };
 
-// Work unit u -> (expert, n-tile, m-tile of this CTA); e advances monotonically with u.
-// A unit is CL m-tiles of one (expert, n-tile), one per CTA of the cluster (rank r
-// takes m = CL*mp + r; m >= the expert's m-tile count is a dummy tile).
-template <int CL>
+// Tile t -> (expert, n-tile, m-tile); e advances monotonically with t.
 struct TileCursor {
   int e = 0;
   template <class S>
-  MOE_DEV bool locate(const S& s, int E, int n_tiles, int u, int rank, int& n, int& m, int& mt) {
-    while (e < E && u >= s.cum[e + 1]) ++e;
+  MOE_DEV bool locate(const S& s, int E, int n_tiles, int t, int& n, int& m) {
+    while (e < E && t >= s.cum[e + 1]) ++e;
     if (e >= E) return false;
-    const int local = u - s.cum[e];
-    mt = (s.poff[e + 1] - s.poff[e]) >> 7;
-    const int mp_count = (mt + CL - 1) / CL;
-    n = local / mp_count;
-    m = (local - n * mp_count) * CL + rank;
+    const int local = t - s.cum[e];
+    const int mt = (s.poff[e + 1] - s.poff[e]) >> 7;
+    n = local / mt;
+    m = local - n * mt;
     return true;
   }
 };
 
-template <int KIND, int BN, int CL>
+template <int KIND, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                         const GemmParams p) {
@@ -157,11 +150,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       s.bad_offsets = 1;
   }
   if (warp == 0) {
-    // work units per expert = ceil(m-tiles / CL) * n-tiles; exclusive scan over experts
+    // tiles per expert = m-tiles * n-tiles; exclusive scan over experts
     int run = 0;
     for (int e0 = 0; e0 < p.E; e0 += 32) {
       const int e = e0 + lane;
-      const int v = e < p.E ? ((max(s.poff[e + 1] - s.poff[e], 0) >> 7) + CL - 1) / CL * p.n_tiles : 0;
+      const int v = e < p.E ? (max(s.poff[e + 1] - s.poff[e], 0) >> 7) * p.n_tiles : 0;
       int incl = v;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -178,7 +171,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // full: operand bytes + the producer's arrival + both copiers' commits (their
       // scale copies are done), so the MMA warp waits on one barrier per stage
       mbar_init(&s.full[i], 3);
-      mbar_init(&s.empty[i], CL);  // one MMA commit from each CTA of the cluster
+      mbar_init(&s.empty[i], 1);
       mbar_init(&s.sf_full[i], 1);
     }
     mbar_init(&s.tfull, 1);
@@ -196,17 +189,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
   const bool bad = s.bad_offsets != 0;
   if (bad && threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE_INDEX);
-  const int total_tiles = bad ? 0 : s.cum[p.E];  // work units
-  const int unit0 = CL == 1 ? (int)blockIdx.x : (int)cluster_id_x();
-  const int unit_step = CL == 1 ? (int)gridDim.x : (int)nclusters_x();
-  const int rank = CL == 1 ? 0 : (int)cluster_ctarank();
-  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1);
+  const int total_tiles = bad ? 0 : s.cum[p.E];
   const int nkb = (p.Kred + 255) >> 8;
   const int ksf4 = p.Kred >> 6;  // scale atoms per 128 rows
 
@@ -219,12 +207,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool issued[kStages];
       for (int i = 0; i < kStages; ++i) issued[i] = false;
       bool ok = true;
-      TileCursor<CL> cur;
-      for (int t = unit0; t < total_tiles && ok; t += unit_step) {
-        int n, m, mt;
-        if (!cur.locate(s, p.E, p.n_tiles, t, rank, n, m, mt)) break;
+      TileCursor cur;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        int n, m;
+        if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
         const int e = cur.e;
-        const int row_a = s.poff[e] + (m < mt ? m : 0) * kBM;  // a dummy tile reads the expert's first rows
+        const int row_a = s.poff[e] + m * kBM;
         const uint8_t* sfa_src = p.a_sf + ((int64_t)(row_a >> 7) * ksf4) * 512;
         // prepared weight row blocks n*kBlocks .. n*kBlocks + kBlocks - 1 of expert e
         const uint8_t* sfb_src =
@@ -236,34 +224,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&s.sf_full[stage], (1 + C::kBlocks) * natoms * 512);
           const int x = kb * kBKBytes;
           tma_load_2d(s.a[stage], &tmap_a, &s.full[stage], x, row_a);
-          // weight block j (128 rows): with a cluster each CTA loads the blocks j = rank
-          // (mod CL) and multicasts them (and their scale atoms) to the whole cluster
 #pragma unroll
-          for (int j = 0; j < C::kBlocks; ++j) {
-            if (CL > 1 && j % CL != rank) continue;
+          for (int j = 0; j < C::kBlocks; ++j) {  // weight block j (128 rows)
             uint8_t* dst = s.b[stage] + j * 128 * kBKBytes;
             if (kL1) {
               // 64 gate rows then the matching 64 up rows (h columns n*BN/2 + 64 j ..)
               const int yb = e * p.b_rows + n * (BN / 2) + 64 * j;
-              if (CL > 1) {
-                tma_load_2d_mc(dst, &tmap_b, &s.full[stage], x, yb, kMask);
-                tma_load_2d_mc(dst + 64 * kBKBytes, &tmap_b, &s.full[stage], x, yb + p.I, kMask);
-              } else {
-                tma_load_2d(dst, &tmap_b, &s.full[stage], x, yb);
-                tma_load_2d(dst + 64 * kBKBytes, &tmap_b, &s.full[stage], x, yb + p.I);
-              }
+              tma_load_2d(dst, &tmap_b, &s.full[stage], x, yb);
+              tma_load_2d(dst + 64 * kBKBytes, &tmap_b, &s.full[stage], x, yb + p.I);
             } else {
-              const int yb = e * p.b_rows + n * BN + 128 * j;
-              if (CL > 1)
-                tma_load_2d_mc(dst, &tmap_b, &s.full[stage], x, yb, kMask);
-              else
-                tma_load_2d(dst, &tmap_b, &s.full[stage], x, yb);
+              tma_load_2d(dst, &tmap_b, &s.full[stage], x, e * p.b_rows + n * BN + 128 * j);
             }
-            const uint8_t* sfb_j = sfb_src + (int64_t)j * ksf4 * 512 + kb * 4 * 512;
-            if (CL > 1)
-              bulk_load_mc(s.sfb[stage] + j * 4 * 512, sfb_j, natoms * 512, &s.sf_full[stage], kMask);
-            else
-              bulk_load(s.sfb[stage] + j * 4 * 512, sfb_j, natoms * 512, &s.sf_full[stage]);
+            bulk_load(s.sfb[stage] + j * 4 * 512, sfb_src + (int64_t)j * ksf4 * 512 + kb * 4 * 512, natoms * 512,
+                      &s.sf_full[stage]);
           }
           bulk_load(s.sfa[stage], sfa_src + kb * 4 * 512, natoms * 512, &s.sf_full[stage]);
           issued[stage] = true;
@@ -285,7 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       int it = 0;
       const uint64_t da0 = sdesc_sw128(s.a[0]), db0 = sdesc_sw128(s.b[0]);
-      for (int t = unit0; t < total_tiles && ok; t += unit_step, ++it) {
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++it) {
         if (!wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb) {
@@ -301,10 +274,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int kk = 0; kk < natoms; ++kk)
             tc_mma_fp4(tmem, da + 2 * kk, db + 2 * kk, C::kIdesc, sf + 4 * kk, sf + 16 + C::kSfbPerStep * kk,
                        (kb | kk) != 0);
-          if (CL > 1)
-            tc_commit_mc(&s.empty[stage], kMask);  // the stage's B half came from the peer too
-          else
-            tc_commit(&s.empty[stage]);
+          tc_commit(&s.empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -323,7 +293,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       const uint64_t dsa0 = sdesc_sf(s.sfa[0]), dsb0 = sdesc_sf(s.sfb[0]);
-      for (int t = unit0; t < total_tiles; t += unit_step) {
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           const int natoms = min(4, ksf4 - 4 * kb);
@@ -355,13 +325,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;
     constexpr int kCols = BN / 2;              // accumulator columns per epilogue warp
     int it = 0;
-    TileCursor<CL> cur;
+    TileCursor cur;
     float amax = 0.0f;
-    for (int t = unit0; t < total_tiles; t += unit_step, ++it) {
-      int n, m, mt;
-      if (!cur.locate(s, p.E, p.n_tiles, t, rank, n, m, mt)) break;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      int n, m;
+      if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
       const int e = cur.e;
-      const bool valid = m < mt && m * kBM + row < s.cnt[e];
+      const bool valid = m * kBM + row < s.cnt[e];
       const int64_t prow = (int64_t)s.poff[e] + m * kBM + row;
       if (!wait_bar_bounded(&s.tfull, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
@@ -509,74 +479,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // no multicast or remote arrive may target an exited CTA
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
-// Grid: one CTA per SM; with CL > 1, as many clusters as can be resident at once
-// (clusters must fit inside a GPC, so that can be fewer than SMs / CL).
-template <int KIND, int BN, int CL>
+template <int KIND, int BN>
 static moe_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st,
                             bool pdl) {
   constexpr size_t kSmemBytes = sizeof(GemmSmem<BN>) + 1024;
-  static int grid = 0;
-  if (!grid) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return MOE_ERR_CUDA;
-    int g = num_sms();
-    if (CL > 1) {
-      cudaLaunchConfig_t q{};
-      q.gridDim = dim3((g / CL) * CL);
-      q.blockDim = dim3(kGemmThreads);
-      q.dynamicSmemBytes = kSmemBytes;
-      cudaLaunchAttribute ca;
-      ca.id = cudaLaunchAttributeClusterDimension;
-      ca.val.clusterDim.x = CL;
-      ca.val.clusterDim.y = 1;
-      ca.val.clusterDim.z = 1;
-      q.attrs = &ca;
-      q.numAttrs = 1;
-      int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<KIND, BN, CL>, &q) != cudaSuccess ||
-          clusters < 1)
-        return MOE_ERR_CUDA;
-      g = std::min(clusters, g / CL) * CL;
-    }
-    grid = g;
+    configured = true;
   }
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  if (CL > 1) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = CL;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-  }
-  if (pdl) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<KIND, BN, CL>, ta, tb, p) == cudaSuccess ? MOE_OK
-                                                                                                : MOE_ERR_CUDA;
+  return launch_ex(grouped_gemm_kernel<KIND, BN>, num_sms(), kGemmThreads, kSmemBytes, st, pdl, ta, tb, p) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 template <int KIND>
 static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int bn,
                               cudaStream_t st, bool pdl) {
-  return bn == 256 ? launch_bn<KIND, 256, TILED_CLUSTER>(ta, tb, p, st, pdl) : launch_bn<KIND, 128, 1>(ta, tb, p, st, pdl);
+  return bn == 256 ? launch_bn<KIND, 256>(ta, tb, p, st, pdl) : launch_bn<KIND, 128>(ta, tb, p, st, pdl);
 }
 
 static int g_policy = MOE_GEMM_AUTO;

@@ -235,6 +235,52 @@ __global__ void prepare_weight_sf_kernel(const uint8_t* __restrict__ src, uint8_
   }
 }
 
+// ---------------------------------------------------------------------------
+// out[t] = bf16(sum_j w[t, j] * y[pair_slot[t, j]]) over j ascending, in fp32 (each
+// product and each sum rounded), pairs with slot -1 skipped; 8 columns per thread.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restrict__ y, int64_t ld_vec,
+                                                           const int32_t* __restrict__ pair_slot,
+                                                           const float* __restrict__ w, int topk, int64_t T,
+                                                           int vec_per_row, int64_t capacity, uint4* __restrict__ out,
+                                                           int32_t* status) {
+  griddep_wait();
+  const int64_t total = T * vec_per_row;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t t = i / vec_per_row;
+    const int64_t v = i - t * vec_per_row;
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+    for (int j = 0; j < topk; ++j) {
+      const int32_t s = __ldg(pair_slot + t * topk + j);
+      if (s < 0) continue;
+      if (s >= capacity) {
+        set_status(status, MOE_ERR_DEVICE_INDEX);
+        continue;
+      }
+      const float wj = __ldg(w + t * topk + j);
+      const uint4 q = __ldg(y + (int64_t)s * ld_vec + v);
+      const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[2 * c] = __fadd_rn(acc[2 * c], __fmul_rn(wj, bf16lo(qw[c])));
+        acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], __fmul_rn(wj, bf16hi(qw[c])));
+      }
+    }
+    out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                        pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+cudaError_t launch_combine(const void* y, int64_t ld_y, const int32_t* pair_slot, const float* w, int topk, int64_t T,
+                           int K, int64_t capacity, void* out, int32_t* status, int blocks, cudaStream_t st,
+                           bool pdl) {
+  return launch_ex(combine_rows_kernel, blocks, 256, 0, st, pdl, reinterpret_cast<const uint4*>(y), ld_y / 8,
+                   pair_slot, w, topk, T, K / 8, capacity, reinterpret_cast<uint4*>(out), status);
+}
+
 cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st, bool pdl) {
   return launch_ex(cast_f32_bf16_kernel, blocks, 256, 0, st, pdl, reinterpret_cast<const float4*>(in),
                    reinterpret_cast<uint4*>(out), n8);

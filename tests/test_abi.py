@@ -70,6 +70,9 @@ def test_argument_checks_fail_before_any_device_work(B):
     assert lib.moe_grouped_gemm_l1(null, null, null, null, null, 1, 128, 256, 128, null, null, null, null, 0,
                                    null, null, null, null, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_cast_output(null, null, 4, 7, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_rows(null, 8, null, null, 4, 2, 7, 16, null, null, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_rows(null, 8, null, null, 4, 2, 8, 16, null, null, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_rows(null, 8, null, null, 0, 2, 8, 16, null, null, null) == B.MOE_OK  # nothing to do
     w = B.MoeWeights()
     assert lib.moe_forward(null, 4, 256, 100, 8, null, null, 2, 0, ctypes.byref(w), null, 0, null, null, null,
                            null, 0, null) in (B.MOE_ERR_INVALID_ARG, B.MOE_ERR_UNSUPPORTED_SHAPE)
