@@ -74,8 +74,10 @@ def dist_setup(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+        gpu = torch.cuda.is_available()
+        if gpu:
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if args.impl == "ours" and gpu else "gloo")
     return ws, rank, local
 
 
@@ -89,7 +91,8 @@ def max_over_ranks(v, ws):
     if ws == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
