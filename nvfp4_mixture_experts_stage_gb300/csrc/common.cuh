@@ -71,8 +71,9 @@ MOE_DEV float e4m3_value(uint32_t b) {
   return float(v);
 }
 
-// Two non-negative fp32 -> one byte of E2M1 magnitude codes (lo = first
-// element, bits 2..0; hi = second element, bits 6..4), RNE, saturating at 6.
+// Two fp32 -> one byte of E2M1 sign-magnitude codes (lo = first element, bits 3..0;
+// hi = second element, bits 7..4), magnitude RNE saturating at 6, sign kept (also
+// for a value that rounds to zero).
 MOE_DEV uint32_t e2m1x2(float lo, float hi) {
   uint16_t r;
   asm("{\n\t.reg .b8 t;\n\t"
@@ -80,11 +81,6 @@ MOE_DEV uint32_t e2m1x2(float lo, float hi) {
       "cvt.u16.u8 %0, t;\n\t}"
       : "=h"(r) : "f"(lo), "f"(hi));
   return r;
-}
-
-// Sign bits of two fp32 placed at bit 3 (lo) and bit 7 (hi) of a code byte.
-MOE_DEV uint32_t sign_bits2(float lo, float hi) {
-  return ((__float_as_uint(lo) >> 31) << 3) | ((__float_as_uint(hi) >> 31) << 7);
 }
 
 // Block scale byte and the reciprocal of its decoded value (0 if the scale is 0).
@@ -96,8 +92,9 @@ MOE_DEV uint32_t block_scale(float bm, float rg, float& rb) {
   return sb;
 }
 
-// Scaled code magnitude (|x|*rg)*rb.  With a zero block scale rb = 0 and the
-// result is 0 (|x|*rg is then tiny, never infinite), leaving sign-only nibbles.
+// Scaled code value (x*rg)*rb; for a magnitude |x| this is the code magnitude, for a
+// signed x it equals sign(x) times it exactly.  With a zero block scale rb = 0 and
+// the result is a signed zero (x*rg is then tiny, never infinite).
 MOE_DEV float code_mag(float ax, float rg, float rb) {
   return __fmul_rn(__fmul_rn(ax, rg), rb);
 }

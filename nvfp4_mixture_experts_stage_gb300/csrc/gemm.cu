@@ -418,10 +418,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               uint32_t w0 = 0, w1 = 0;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                uint32_t b0 = e2m1x2(code_mag(fabsf(h[2 * i]), rg, rb), code_mag(fabsf(h[2 * i + 1]), rg, rb)) |
-                              sign_bits2(h[2 * i], h[2 * i + 1]);
-                uint32_t b1 = e2m1x2(code_mag(fabsf(h[8 + 2 * i]), rg, rb), code_mag(fabsf(h[8 + 2 * i + 1]), rg, rb)) |
-                              sign_bits2(h[8 + 2 * i], h[8 + 2 * i + 1]);
+                // signed (h*rg)*rb: the conversion keeps the sign, also of a zero code
+                uint32_t b0 = e2m1x2(code_mag(h[2 * i], rg, rb), code_mag(h[2 * i + 1], rg, rb));
+                uint32_t b1 = e2m1x2(code_mag(h[8 + 2 * i], rg, rb), code_mag(h[8 + 2 * i + 1], rg, rb));
                 w0 |= b0 << (8 * i);
                 w1 |= b1 << (8 * i);
               }

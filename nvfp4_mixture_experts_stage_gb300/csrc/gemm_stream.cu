@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   for (int i = 0; i < 4; ++i) {
                     const float lo = h[16 * b + 8 * w4 + 2 * i], hi = h[16 * b + 8 * w4 + 2 * i + 1];
                     const uint32_t byte =
-                        e2m1x2(code_mag(fabsf(lo), rg, rb), code_mag(fabsf(hi), rg, rb)) | sign_bits2(lo, hi);
+                        e2m1x2(code_mag(lo, rg, rb), code_mag(hi, rg, rb));  // signed: sign kept
                     word |= byte << (8 * i);
                   }
                   cw[2 * b + w4] = word;

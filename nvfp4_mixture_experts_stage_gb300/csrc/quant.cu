@@ -74,6 +74,10 @@ template <int DST>
 __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
   griddep_wait();  // everything read below comes from earlier kernels
   griddep_launch_dependents();
+  // 1/decode(b) for every block-scale byte b (scales are non-negative and <= 448, so
+  // b <= 0x7E; b = 0 gives 0): the same values the per-block reciprocal would give
+  __shared__ float s_rb[128];
+  if (threadIdx.x < 128) s_rb[threadIdx.x] = threadIdx.x ? __frcp_rn(e4m3_value(threadIdx.x)) : 0.0f;
   float amax_f = 0.0f;
   if (!a.gs_fixed) {
     if (a.amax_partials) {  // reduce the per-block maxima (non-negative: bits order like values)
@@ -87,13 +91,17 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
   const float gs = a.gs_fixed ? __ldg(a.gs_fixed) : __fdiv_rn(amax_f, kGsDivisor);
   const float rg = recip_global_scale(gs);
   if (a.gs_out && blockIdx.x == 0 && threadIdx.x == 0) *a.gs_out = gs;
+  __syncthreads();
 
   const int lane = threadIdx.x & 31;
-  // segment index s -> (row, segment); 32-bit (the host keeps rows*nseg < 2^31)
+  // segment s (256 elements of one row) -> (row, seg); a warp takes segments warp0,
+  // warp0 + nwarps, ...: row and seg advance incrementally (no division in the loop)
   const uint32_t nseg = (uint32_t)((a.K + 255) >> 8);
   const uint32_t total = (uint32_t)(a.rows * nseg);
   const uint32_t warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const uint32_t drow = nwarps / nseg, dseg = nwarps - drow * nseg;
+  uint32_t cur_row = warp0 / nseg, cur_seg = warp0 - cur_row * nseg;
   const int k_sf = a.K >> 4;
   const int half_k = a.K >> 1;
 
@@ -105,9 +113,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t s = base + u * nwarps;
-      const uint32_t r = s / nseg;
-      row[u] = r;
-      col[u] = (int)(s - r * nseg) * 256 + lane * 8;  // first element of this lane
+      row[u] = cur_row;
+      col[u] = (int)cur_seg * 256 + lane * 8;  // first element of this lane
+      cur_row += drow;
+      cur_seg += dseg;
+      if (cur_seg >= nseg) { cur_seg -= nseg; ++cur_row; }
       bool ok = s < total && col[u] < a.K;
       if (ok && DST == kDstMasked) ok = __ldg(a.slot_token + row[u]) >= 0;
       v[u] = ok ? __ldcs(a.x + row[u] * a.ld_vec + (col[u] >> 3)) : make_uint4(0, 0, 0, 0);
@@ -132,16 +142,14 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
       const float bm = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      float rb;
-      const uint32_t sb = block_scale(bm, rg, rb);
+      const uint32_t sb = e4m3_byte(__fdiv_rn(__fmul_rn(bm, rg), 6.0f));
+      const float rb = s_rb[sb];
+      // (x*rg)*rb is sign(x) * ((|x|*rg)*rb) exactly, and the E2M1 conversion rounds
+      // the magnitude and keeps the sign (also of a value that rounds to zero)
       uint32_t code = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = f[2 * i], hi = f[2 * i + 1];
-        uint32_t byte = e2m1x2(code_mag(fabsf(lo), rg, rb), code_mag(fabsf(hi), rg, rb));
-        byte |= sign_bits2(lo, hi);
-        code |= byte << (8 * i);
-      }
+      for (int i = 0; i < 4; ++i)
+        code |= e2m1x2(__fmul_rn(__fmul_rn(f[2 * i], rg), rb), __fmul_rn(__fmul_rn(f[2 * i + 1], rg), rb)) << (8 * i);
       // scale word of 4 blocks, assembled on lane 8j from lanes 8j, 8j+2, 8j+4, 8j+6
       const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
       const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
