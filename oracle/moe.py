@@ -189,6 +189,43 @@ def forward(x, topk_ids, topk_w, E, expert_offset, weights, gs_x=None, gs_h=None
     }
 
 
+def forward_bf16(x, topk_ids, topk_w, E, expert_offset, expert_w1, expert_w2, tokens=None):
+    """The same layer without NVFP4 quantisation: the BF16 reference the pages
+    compare the NVFP4 layer against (cosine similarity of the outputs).
+
+    g = bf16(x @ W1_gate^T), u = bf16(x @ W1_up^T), h = bf16(silu(g) * u),
+    y = bf16(h @ W2^T), out[t] = bf16(sum_j w[t, j] * y_j) in pair order, with the
+    contractions in fp64 (rounded to fp32) and the BF16 rounding points of the
+    quantised layer.  expert_w1(e) -> [2I, K], expert_w2(e) -> [K, I] (BF16 values
+    as fp32); only the experts the chosen tokens route to are requested.
+    Returns out [len(tokens), K] float32."""
+    x = np.asarray(x, np.float32)
+    T, K = x.shape
+    topk = topk_ids.shape[1]
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens)
+    w = np.asarray(topk_w, np.float32).reshape(T, topk)
+    loc = np.asarray(topk_ids, np.int64).reshape(T, topk) - expert_offset
+    cache = {}
+    out = np.zeros((len(tokens), K), np.float32)
+    for i, t in enumerate(tokens):
+        acc = np.zeros(K, np.float32)
+        for j in range(topk):
+            e = int(loc[t, j])
+            if not 0 <= e < E:
+                continue
+            if e not in cache:
+                cache[e] = (np.asarray(expert_w1(e), np.float64), np.asarray(expert_w2(e), np.float64))
+            w1, w2 = cache[e]
+            I = w1.shape[0] // 2
+            gu = (w1 @ x[t].astype(np.float64)).astype(np.float32)
+            g, u = nvfp4.bf16_round(gu[:I]), nvfp4.bf16_round(gu[I:])
+            h = silu_mul(g, u)
+            y = nvfp4.bf16_round((w2 @ h.astype(np.float64)).astype(np.float32))
+            acc = acc + w[t, j] * y
+        out[i] = nvfp4.bf16_round(acc)
+    return out
+
+
 def quantize_weights(w1, w2):
     """Quantise BF16 expert weights the way the layer consumes them.
 
