@@ -44,7 +44,8 @@ NCU_TRAFFIC = {"gemm_l1": {"bytes": 673994496, "sources_sha256_16": "a9b70436629
 def gemm_sources_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm_stream.cu", "tcgen05.cuh", "kernels.cuh", "common.cuh"):
+    for f in ("gemm.cu", "gemm_pair.cu", "gemm_tiled.cuh", "gemm_stream.cu", "tcgen05.cuh", "kernels.cuh",
+              "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_stage_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -61,7 +62,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other workloads of the table (prefill, skewed routing) after the headline")
-    ap.add_argument("--gemm-policy", default="auto", choices=["auto", "tiled", "stream", "stream32", "stream64"],
+    ap.add_argument("--gemm-policy", default="auto",
+                    choices=["auto", "tiled", "tiled1", "tiledp", "stream", "stream32", "stream64"],
                     help="grouped-GEMM kernel selection (moe_set_gemm_policy)")
     ap.add_argument("--profile-only", action="store_true",
                     help="run warm-up + steps of the fixed-gs layer and exit (for ncu); prints nothing")
@@ -301,7 +303,9 @@ def run_ours(args, ws, rank, local):
     build.build()
     from nvfp4_mixture_experts_stage_gb300 import binding as B, runtime as R
 
-    B.moe_set_gemm_policy({"auto": B.MOE_GEMM_AUTO, "tiled": B.MOE_GEMM_TILED, "stream": B.MOE_GEMM_STREAMING,
+    B.moe_set_gemm_policy({"auto": B.MOE_GEMM_AUTO, "tiled": B.MOE_GEMM_TILED, "tiled1": B.MOE_GEMM_TILED_1CTA,
+                           "tiledp": B.MOE_GEMM_TILED_PAIR,
+                           "stream": B.MOE_GEMM_STREAMING,
                            "stream32": B.MOE_GEMM_STREAMING_N32,
                            "stream64": B.MOE_GEMM_STREAMING_N64}[args.gemm_policy])
     wl = workloads.WORKLOADS[args.workload]

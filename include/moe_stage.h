@@ -262,9 +262,15 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const 
  *                      implies at most 64 slots per local expert on average
  *                      (capacity - 127*E <= 64*E) and the contraction is <= 4096,
  *                      the tiled kernel otherwise;
- *   MOE_GEMM_TILED     always the tiled kernel: 128 slot rows x 256 weight rows per
- *                      tile (128 where I % 128 or, for L2, K % 256 leaves no
- *                      choice), slots on the MMA's M side;
+ *   MOE_GEMM_TILED     always a tiled kernel, slots on the MMA's M side: L1 in tiles
+ *                      of 128 slot rows x 256 weight rows on single SMs; L2 in tiles
+ *                      of 256 slot rows x 256 weight rows on pairs of SMs (a cluster
+ *                      of two CTAs sharing one M=256 MMA: each SM stages its own 128
+ *                      slot rows and half of the weight rows); 128 x 128 tiles on
+ *                      single SMs where I % 128 or, for L2, K % 256 leaves no choice;
+ *   MOE_GEMM_TILED_1CTA the tiled kernels on single SMs only;
+ *   MOE_GEMM_TILED_PAIR the tiled kernels with 256-wide tiles on SM pairs for both
+ *                      GEMMs;
  *   MOE_GEMM_STREAMING the weight-streaming kernel whenever the contraction is
  *                      <= 4096: weight rows on the MMA's M side, chunks of slots on
  *                      its N side, the chunk's activation scales resident in tensor
@@ -273,13 +279,15 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const 
  *                      back for each weight block, so the repeated weight reads come
  *                      from L2.  The chunk is 32 slots (8 pipeline stages fit);
  *   MOE_GEMM_STREAMING_N32 / _N64  the streaming kernel with the chunk forced.
- * Both kernels compute the same arithmetic (results may differ in the fp32
+ * All kernels compute the same arithmetic (results may differ in the fp32
  * summation order only). */
 #define MOE_GEMM_AUTO           0
 #define MOE_GEMM_TILED          1
 #define MOE_GEMM_STREAMING      2
 #define MOE_GEMM_STREAMING_N32  3
 #define MOE_GEMM_STREAMING_N64  4
+#define MOE_GEMM_TILED_1CTA     5
+#define MOE_GEMM_TILED_PAIR     6
 int moe_set_gemm_policy(int policy);
 
 /* out_bf16[i] = bf16(out32[i]) for i < T*K (round to nearest even). */

@@ -41,7 +41,7 @@ EXPORTS = (
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
-MOE_GEMM_STREAMING_N32, MOE_GEMM_STREAMING_N64 = 3, 4
+MOE_GEMM_STREAMING_N32, MOE_GEMM_STREAMING_N64, MOE_GEMM_TILED_1CTA, MOE_GEMM_TILED_PAIR = 3, 4, 5, 6
 
 MOE_ROUTE_STATIC_TABLE_INTS = 262144
 
@@ -136,8 +136,9 @@ def moe_workspace_size(T_max, K, I, E, topk):
 
 
 def moe_set_gemm_policy(policy):
-    """Select the grouped-GEMM kernel (MOE_GEMM_AUTO / _TILED / _STREAMING);
-    returns the previous policy."""
+    """Select the grouped-GEMM kernels (MOE_GEMM_AUTO / _TILED / _TILED_1CTA /
+    _TILED_PAIR / _STREAMING / _STREAMING_N32 / _STREAMING_N64); returns the
+    previous policy."""
     r = _lib.moe_set_gemm_policy(policy)
     if r < 0:
         raise MoeError("moe_set_gemm_policy", MOE_ERR_INVALID_ARG)

@@ -144,7 +144,7 @@ const char* moe_status_string(moe_status s) {
 }
 
 int moe_set_gemm_policy(int policy) {
-  if (policy < MOE_GEMM_AUTO || policy > MOE_GEMM_STREAMING_N64) return -1;
+  if (policy < MOE_GEMM_AUTO || policy > MOE_GEMM_TILED_PAIR) return -1;
   return set_gemm_policy(policy);
 }
 

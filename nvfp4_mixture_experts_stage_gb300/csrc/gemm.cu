@@ -30,15 +30,9 @@
 // Tiles are (expert, n-tile, m-tile), m fastest, dealt round-robin over the CTAs, so
 // CTAs running at the same time share weight tiles through L2; the expert of a tile
 // comes from the padded offsets on the device (no host sync).
-#include "tcgen05.cuh"
+#include "gemm_tiled.cuh"
 
 namespace moe {
-
-constexpr int kBM = 128;
-constexpr int kBKBytes = 128;               // 256 fp4 per row per stage
-constexpr int kGemmThreads = 384;
-constexpr int kEpiWarps = 8;
-constexpr int kTmemCols = 512;
 
 template <int BN>
 struct TiledCfg {
@@ -54,36 +48,6 @@ struct TiledCfg {
   static constexpr uint32_t kIdesc =
       (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
   static_assert(kSfBase + kStages * kSfCols <= kTmemCols, "tensor memory budget");
-};
-
-enum GemmKind : int { kL1GateUp = 0, kL1Silu = 1, kL1Requant = 2, kL2Rows = 3, kL2Scatter = 4 };
-
-struct GemmParams {
-  const uint8_t* a_sf;              // swizzled [cap/128][Kred/64][512]
-  const uint8_t* b_sf;              // prepared [E][rows_per_expert/128][Kred/64][512]
-  const int32_t* offsets;           // [E+1]
-  const int32_t* padded_offsets;    // [E+1]
-  int E;
-  int Kred;                         // contraction length in elements
-  int n_tiles;                      // output tiles per expert
-  int b_rows;                       // weight rows per expert
-  int I;                            // L1: columns of gate (= of up)
-  const float* gs_a;
-  const float* gs_b0;               // L1 gate / L2 down
-  const float* gs_b1;               // L1 up
-  void* out_bf16;
-  int64_t out_ld;                   // elements per output row
-  float* h_amax;
-  uint8_t* h_fp4;
-  uint8_t* h_sf;
-  const float* gs_h;
-  const int32_t* slot_token;
-  const float* slot_weight;
-  float* out32;
-  int64_t T;
-  int out_cols;                     // L2: K
-  int64_t cap;                      // slot rows of A (bound for the offsets)
-  int32_t* status;
 };
 
 template <int BN>
@@ -107,21 +71,6 @@ struct __align__(1024) GemmSmem {
   int cum[257];                     // tiles before expert e
 };
 
-// Tile t -> (expert, n-tile, m-tile); e advances monotonically with t.
-struct TileCursor {
-  int e = 0;
-  template <class S>
-  MOE_DEV bool locate(const S& s, int E, int n_tiles, int t, int& n, int& m) {
-    while (e < E && t >= s.cum[e + 1]) ++e;
-    if (e >= E) return false;
-    const int local = t - s.cum[e];
-    const int mt = (s.poff[e + 1] - s.poff[e]) >> 7;
-    n = local / mt;
-    m = local - n * mt;
-    return true;
-  }
-};
-
 template <int KIND, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -137,35 +86,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   griddep_wait();
   griddep_launch_dependents();
-  if (threadIdx.x == 0) s.bad_offsets = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s.poff[i] = p.padded_offsets[i];
-  for (int i = threadIdx.x; i < p.E; i += blockDim.x) s.cnt[i] = p.offsets[i + 1] - p.offsets[i];
-  __syncthreads();
-  // the tile walk trusts the offsets: check them once (monotone, 128-aligned,
-  // counts within their padded ranges, inside the slot capacity)
-  for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
-    const int lo = s.poff[i], hi = s.poff[i + 1], c = s.cnt[i];
-    if (lo < 0 || hi < lo || (lo & 127) || (hi & 127) || c < 0 || c > hi - lo || hi > p.cap)
-      s.bad_offsets = 1;
-  }
-  if (warp == 0) {
-    // tiles per expert = m-tiles * n-tiles; exclusive scan over experts
-    int run = 0;
-    for (int e0 = 0; e0 < p.E; e0 += 32) {
-      const int e = e0 + lane;
-      const int v = e < p.E ? (max(s.poff[e + 1] - s.poff[e], 0) >> 7) * p.n_tiles : 0;
-      int incl = v;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += t;
-      }
-      if (e < p.E) s.cum[e] = run + incl - v;
-      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    }
-    if (lane == 0) s.cum[p.E] = run;
-  }
+  build_tile_table(s, p, 1);
   if (threadIdx.x == 32) {
     for (int i = 0; i < kStages; ++i) {
       // full: operand bytes + the producer's arrival + both copiers' commits (their
@@ -210,7 +131,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       TileCursor cur;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         int n, m;
-        if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
+        if (!cur.locate(s, p.E, 1, t, n, m)) break;
         const int e = cur.e;
         const int row_a = s.poff[e] + m * kBM;
         const uint8_t* sfa_src = p.a_sf + ((int64_t)(row_a >> 7) * ksf4) * 512;
@@ -329,151 +250,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float amax = 0.0f;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       int n, m;
-      if (!cur.locate(s, p.E, p.n_tiles, t, n, m)) break;
+      if (!cur.locate(s, p.E, 1, t, n, m)) break;
       const int e = cur.e;
       const bool valid = m * kBM + row < s.cnt[e];
       const int64_t prow = (int64_t)s.poff[e] + m * kBM + row;
       if (!wait_bar_bounded(&s.tfull, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-      // L1: columns of this warp's gate values and of the matching up values; L2: kCols
-      // consecutive output columns
       float v[kCols];
-      if constexpr (kL1) {
-        // BN 256: half h = prepared block h (gate at 128h, up at 128h + 64), 64 columns each;
-        // BN 128: half h = gate columns 32h.., up columns 64 + 32h..
-        constexpr int G = kCols / 2;
-        const uint32_t g0 = BN == 256 ? 128 * half : 32 * half;
-        if constexpr (G == 64) {
-          tmem_ld64(taddr + g0, *reinterpret_cast<float(*)[64]>(&v[0]));
-          tmem_ld64(taddr + g0 + 64, *reinterpret_cast<float(*)[64]>(&v[G]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < G; j += 16) {
-            tmem_ld16(taddr + g0 + j, *reinterpret_cast<float(*)[16]>(&v[j]));
-            tmem_ld16(taddr + g0 + 64 + j, *reinterpret_cast<float(*)[16]>(&v[G + j]));
-          }
-        }
-      } else {
-        if constexpr (kCols % 64 == 0) {
-#pragma unroll
-          for (int j = 0; j < kCols; j += 64)
-            tmem_ld64(taddr + half * kCols + j, *reinterpret_cast<float(*)[64]>(&v[j]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < kCols; j += 16)
-            tmem_ld16(taddr + half * kCols + j, *reinterpret_cast<float(*)[16]>(&v[j]));
-        }
-      }
+      epilogue_load<KIND, BN>(taddr, half, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.tempty);  // accumulator free: values are in registers
-
-      if (kL1) {
-        constexpr int G = kCols / 2;           // h columns of this warp
-        const int hcol0 = n * (BN / 2) + (BN == 256 ? 64 * half : 32 * half);
-        const float gs_a = __ldg(p.gs_a);
-        const float ag = __fmul_rn(gs_a, __ldg(p.gs_b0 + e));
-        const float au = __fmul_rn(gs_a, __ldg(p.gs_b1 + e));
-        float rg = 0.0f;
-        if (KIND == kL1Requant) rg = recip_global_scale(__ldg(p.gs_h));
-        uint32_t sfw = 0;
-#pragma unroll
-        for (int c = 0; c < G / 16; ++c) {
-          float g[16], u[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            g[i] = round_bf16(__fmul_rn(ag, v[16 * c + i]));
-            u[i] = round_bf16(__fmul_rn(au, v[G + 16 * c + i]));
-          }
-          const int col = hcol0 + 16 * c;  // h column (gate/up column) of element 0
-          if (KIND == kL1GateUp) {
-            if (valid) {
-              uint4* dg = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
-              uint4* du = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + p.I + col);
-              dg[0] = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
-              dg[1] = make_uint4(pack_bf16x2(g[8], g[9]), pack_bf16x2(g[10], g[11]), pack_bf16x2(g[12], g[13]), pack_bf16x2(g[14], g[15]));
-              du[0] = make_uint4(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]), pack_bf16x2(u[4], u[5]), pack_bf16x2(u[6], u[7]));
-              du[1] = make_uint4(pack_bf16x2(u[8], u[9]), pack_bf16x2(u[10], u[11]), pack_bf16x2(u[12], u[13]), pack_bf16x2(u[14], u[15]));
-            }
-          } else {
-            float h[16];
-            float bm = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              h[i] = silu_mul(g[i], u[i]);
-              bm = fmaxf(bm, fabsf(h[i]));
-            }
-            if (valid) {
-              if (p.out_bf16) {
-                uint4* dh = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
-                dh[0] = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
-                dh[1] = make_uint4(pack_bf16x2(h[8], h[9]), pack_bf16x2(h[10], h[11]), pack_bf16x2(h[12], h[13]), pack_bf16x2(h[14], h[15]));
-              }
-              amax = fmaxf(amax, bm);
-            }
-            if (KIND == kL1Requant) {
-              float rb;
-              const uint32_t sb = block_scale(bm, rg, rb);
-              uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                // signed (h*rg)*rb: the conversion keeps the sign, also of a zero code
-                uint32_t b0 = e2m1x2(code_mag(h[2 * i], rg, rb), code_mag(h[2 * i + 1], rg, rb));
-                uint32_t b1 = e2m1x2(code_mag(h[8 + 2 * i], rg, rb), code_mag(h[8 + 2 * i + 1], rg, rb));
-                w0 |= b0 << (8 * i);
-                w1 |= b1 << (8 * i);
-              }
-              sfw |= sb << (8 * c);
-              if (valid)
-                *reinterpret_cast<uint2*>(p.h_fp4 + prow * (p.I >> 1) + (col >> 1)) = make_uint2(w0, w1);
-            }
-          }
-        }
-        if (KIND == kL1Requant && valid) {
-          // G/16 consecutive scale columns starting at a multiple of 2 (BN 128) or 4 (BN 256)
-          uint8_t* sp = p.h_sf + sf_swizzle_offset(prow, hcol0 >> 4, p.I >> 4);
-          if constexpr (G == 64)
-            *reinterpret_cast<uint32_t*>(sp) = sfw;
-          else
-            *reinterpret_cast<uint16_t*>(sp) = (uint16_t)sfw;
-        }
-      } else {
-        const float alpha = __fmul_rn(__ldg(p.gs_a), __ldg(p.gs_b0 + e));
-        int32_t tok = -1;
-        float wgt = 0.0f;
-        if (KIND == kL2Scatter && valid) {
-          tok = __ldg(p.slot_token + prow);
-          wgt = __ldg(p.slot_weight + prow);
-          if (tok >= p.T) { set_status(p.status, MOE_ERR_DEVICE_INDEX); tok = -1; }
-        }
-#pragma unroll
-        for (int c = 0; c < kCols / 16; ++c) {
-          float y[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) y[i] = round_bf16(__fmul_rn(alpha, v[16 * c + i]));
-          const int col = n * BN + half * kCols + c * 16;
-          if (KIND == kL2Rows) {
-            if (valid) {
-              uint4* dy = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
-              dy[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-              dy[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]), pack_bf16x2(y[12], y[13]), pack_bf16x2(y[14], y[15]));
-            }
-          } else if (tok >= 0) {
-            float4* dst = reinterpret_cast<float4*>(p.out32 + (int64_t)tok * p.out_cols + col);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              atomicAdd(dst + j, make_float4(__fmul_rn(wgt, y[4 * j]), __fmul_rn(wgt, y[4 * j + 1]),
-                                             __fmul_rn(wgt, y[4 * j + 2]), __fmul_rn(wgt, y[4 * j + 3])));
-          }
-        }
-      }
+      epilogue_store<KIND, BN>(p, v, e, n, half, valid, prow, amax);
     }
-    if (KIND == kL1Silu && p.h_amax) {
-      // non-negative floats order like their bit patterns
-      const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
-      if (lane == 0 && mb) atomicMax(reinterpret_cast<uint32_t*>(p.h_amax), mb);
-    }
+    epilogue_finish<KIND>(p, amax);
   }
 
   tc_fence_before();
@@ -513,11 +304,21 @@ int gemm_policy() { return __atomic_load_n(&g_policy, __ATOMIC_RELAXED); }
 
 int set_gemm_policy(int policy) { return __atomic_exchange_n(&g_policy, policy, __ATOMIC_RELAXED); }
 
+// Which GEMM runs its 256-wide tiles on CTA pairs: L2 unless single-CTA tiles are
+// forced (prefill L2 0.38 ms against 0.41 ms); L1 only when forced (0.69 ms against
+// 0.68: the pair computes the empty half of every expert's odd last m-tile).
+bool pair_gemm_enabled(bool l1) {
+  const int pol = gemm_policy();
+  return l1 ? pol == MOE_GEMM_TILED_PAIR : pol != MOE_GEMM_TILED_1CTA;
+}
+
 // Small per-expert slot counts (at most 64 slots per local expert on average even if
 // every pair were local): stream the weights with the slot chunk on the MMA's N side.
 bool use_stream_gemm(int64_t cap, int E, int Kred) {
   const int pol = gemm_policy();
-  if (pol == MOE_GEMM_TILED || !stream_gemm_supported(Kred)) return false;
+  if (pol == MOE_GEMM_TILED || pol == MOE_GEMM_TILED_1CTA || pol == MOE_GEMM_TILED_PAIR ||
+      !stream_gemm_supported(Kred))
+    return false;
   if (pol != MOE_GEMM_AUTO) return true;
   return cap - (int64_t)(kTileM - 1) * E <= (int64_t)64 * E;
 }
@@ -564,6 +365,12 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
     if (cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
     pdl = false;  // the predecessor is now the memset, not a kernel
   }
+  if (bn == 256 && pair_gemm_enabled(true)) {
+    const int kind = epilogue == MOE_L1_GATEUP_BF16 ? kL1GateUp : epilogue == MOE_L1_SILU_BF16 ? kL1Silu : kL1Requant;
+    if (epilogue != MOE_L1_GATEUP_BF16 && epilogue != MOE_L1_SILU_BF16 && epilogue != MOE_L1_SILU_REQUANT)
+      return MOE_ERR_INVALID_ARG;
+    return launch_pair_gemm(kind, ta, tb, p, st, pdl);
+  }
   switch (epilogue) {
     case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, p, bn, st, pdl);
     case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, p, bn, st, pdl);
@@ -606,6 +413,10 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
   p.out_cols = K;
   p.cap = cap;
   p.status = status;
+  if (bn == 256 && pair_gemm_enabled(false)) {
+    if (epilogue != MOE_L2_ROWS_BF16 && epilogue != MOE_L2_SCATTER) return MOE_ERR_INVALID_ARG;
+    return launch_pair_gemm(epilogue == MOE_L2_ROWS_BF16 ? kL2Rows : kL2Scatter, ta, tb, p, st, pdl);
+  }
   switch (epilogue) {
     case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, p, bn, st, pdl);
     case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, p, bn, st, pdl);

@@ -39,6 +39,16 @@ MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+// Tiled 2-D load into this CTA's shared memory whose completion is counted on the
+// mbarrier at cluster address `bar` (from mapa_shared), which may be the peer's of
+// the CTA pair.
+MOE_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
 MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -71,6 +81,69 @@ MOE_DEV void tc_mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint
       "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
+// ---- CTA pairs (a cluster of two CTAs sharing one tcgen05.mma of M = 256) ----
+MOE_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs (aligned: whole warps, uniform control flow).
+MOE_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+MOE_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared), with
+// the default semantics of mbarrier.arrive (release at CTA scope): the hand-off of a
+// drained accumulator to the CTA pair's MMA issuer.  (A release at cluster scope costs
+// about 0.6 us per arrival here: it waits for the SM's outstanding stores.)
+MOE_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Phase test with cluster-scope acquire, for barriers that CTAs of the cluster arrive on.
+MOE_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Commit of the pair's tcgen05 operations issued by this thread: one arrival on the
+// barrier at the same offset in every CTA of cta_mask.
+MOE_DEV void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+// Scale atom copy issued by the leader for both CTAs: each CTA's shared memory at this
+// descriptor into its own TMEM at taddr.
+MOE_DEV void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Block-scaled MMA of the pair (M = 256): A rows 0..127 and 128..255 from the two CTAs'
+// shared memory, B's N rows split in halves between them, D and the A scales in each
+// CTA's own TMEM, the B scales of all N rows in each CTA's TMEM.
+MOE_DEV void tc_mma_fp4_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // 16 consecutive fp32 columns of this thread's TMEM lane; the wait sits in the same
 // asm statement so no use of the outputs can be scheduled before it.
 MOE_DEV void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -133,6 +206,24 @@ MOE_DEV bool wait_bar_bounded(uint64_t* bar, uint32_t parity, int* abort_flag, i
   return true;
 }
 
+// wait_bar_bounded with cluster-scope acquire.
+MOE_DEV bool wait_bar_cluster(uint64_t* bar, uint32_t parity, int* abort_flag, int32_t* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if ((++spins & 255u) == 0) {
+      if (*(volatile int*)abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *(volatile int*)abort_flag = 1;
+        set_status(status, MOE_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 // Wait for a phase with a time limit only (teardown paths).
 MOE_DEV void wait_bar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -173,6 +264,23 @@ inline bool make_tmap(CUtensorMap* map, const void* base, uint64_t row_bytes, ui
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Byte matrix [rows, row_bytes] as a 2-D uint8 tensor map without swizzle, box of
+// box_rows x row_bytes (row_bytes <= 256, a multiple of 16): contiguous runs of
+// scale atoms.
+inline bool make_tmap_plain(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows,
+                            uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -46,6 +46,22 @@ def test_slot_capacity(B):
     assert B.moe_slot_capacity(-1, 1, 1) == -1
 
 
+def test_gemm_policy_values(B):
+    """Every documented policy is accepted and returned as the previous one; others fail."""
+    old = B.moe_set_gemm_policy(B.MOE_GEMM_AUTO)
+    try:
+        for pol in (B.MOE_GEMM_TILED, B.MOE_GEMM_STREAMING, B.MOE_GEMM_STREAMING_N32, B.MOE_GEMM_STREAMING_N64,
+                    B.MOE_GEMM_TILED_1CTA, B.MOE_GEMM_TILED_PAIR, B.MOE_GEMM_AUTO):
+            prev = B.moe_set_gemm_policy(pol)
+            assert B.moe_set_gemm_policy(pol) == pol
+            assert prev != pol or pol == B.MOE_GEMM_AUTO
+        for bad in (-1, 7):
+            with pytest.raises(B.MoeError):
+                B.moe_set_gemm_policy(bad)
+    finally:
+        B.moe_set_gemm_policy(old)
+
+
 def test_workspace_sizes(B):
     assert B.moe_stage_workspace_size() >= 4
     assert B.moe_route_workspace_size(256, 8, 48) >= 2 * 8 * 48 * 4

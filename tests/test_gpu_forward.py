@@ -21,11 +21,13 @@ def _lib():
     B, R = binding, runtime
 
 
-@pytest.fixture(params=["tiled", "stream32", "stream64"], autouse=True)
+@pytest.fixture(params=["tiled", "tiled1", "tiledp", "stream32", "stream64"], autouse=True)
 def gemm_kernel(request, _lib):
-    """Run every test with each grouped-GEMM kernel (and streaming chunk) forced."""
-    pol = {"tiled": B.MOE_GEMM_TILED, "stream32": B.MOE_GEMM_STREAMING_N32,
-           "stream64": B.MOE_GEMM_STREAMING_N64}[request.param]
+    """Run every test with each grouped-GEMM kernel (and streaming chunk) forced:
+    tiled = the default tiled choice (L2's 256-wide tiles on CTA pairs), tiled1 =
+    single-CTA tiles only, tiledp = CTA pairs for both GEMMs' 256-wide tiles."""
+    pol = {"tiled": B.MOE_GEMM_TILED, "tiled1": B.MOE_GEMM_TILED_1CTA, "tiledp": B.MOE_GEMM_TILED_PAIR,
+           "stream32": B.MOE_GEMM_STREAMING_N32, "stream64": B.MOE_GEMM_STREAMING_N64}[request.param]
     old = B.moe_set_gemm_policy(pol)
     yield request.param
     B.moe_set_gemm_policy(old)

@@ -125,6 +125,22 @@ def test_prefill_sampled_tokens(layer, full_weights):
     _sampled(layer, full_weights, wl, tokens)
 
 
+def test_prefill_pair_and_single_cta_tiles_agree(layer):
+    """Every output of the prefill layer: 256-row tiles on CTA pairs against 128-row
+    tiles on single CTAs (same operands, same k order per output)."""
+    wl = workloads.WORKLOADS["prefill"]
+    gs_h = workloads.fixed_gs_h(wl)
+    old = B.moe_set_gemm_policy(B.MOE_GEMM_TILED_PAIR)
+    try:
+        pair, _, _, _, _ = _gpu_forward(layer, wl, B.MOE_GS_FIXED, gs_h=gs_h)
+        B.moe_set_gemm_policy(B.MOE_GEMM_TILED_1CTA)
+        single, _, _, _, _ = _gpu_forward(layer, wl, B.MOE_GS_FIXED, gs_h=gs_h)
+    finally:
+        B.moe_set_gemm_policy(old)
+    assert np.isfinite(pair).all()
+    assert_layer_close(pair, single.astype(np.float64), "pair vs single-CTA tiles")
+
+
 def test_skew_top1_sampled_tokens(layer, full_weights):
     wl = workloads.WORKLOADS["skew_top1"]
     ids, _ = workloads.routing(wl)

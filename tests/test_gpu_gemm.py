@@ -24,11 +24,13 @@ def _lib():
     B = binding
 
 
-@pytest.fixture(params=["tiled", "stream32", "stream64"], autouse=True)
+@pytest.fixture(params=["tiled", "tiled1", "tiledp", "stream32", "stream64"], autouse=True)
 def gemm_kernel(request, _lib):
-    """Run every test with each grouped-GEMM kernel (and streaming chunk) forced."""
-    pol = {"tiled": B.MOE_GEMM_TILED, "stream32": B.MOE_GEMM_STREAMING_N32,
-           "stream64": B.MOE_GEMM_STREAMING_N64}[request.param]
+    """Run every test with each grouped-GEMM kernel (and streaming chunk) forced:
+    tiled = the default tiled choice (L2's 256-wide tiles on CTA pairs), tiled1 =
+    single-CTA tiles only, tiledp = CTA pairs for both GEMMs' 256-wide tiles."""
+    pol = {"tiled": B.MOE_GEMM_TILED, "tiled1": B.MOE_GEMM_TILED_1CTA, "tiledp": B.MOE_GEMM_TILED_PAIR,
+           "stream32": B.MOE_GEMM_STREAMING_N32, "stream64": B.MOE_GEMM_STREAMING_N64}[request.param]
     old = B.moe_set_gemm_policy(pol)
     yield request.param
     B.moe_set_gemm_policy(old)
@@ -38,7 +40,9 @@ POW2_BYTES = np.array([0x28, 0x30, 0x38, 0x40, 0x48], np.uint8)  # 0.25 .. 4
 POW2_BYTES_NARROW = np.array([0x30, 0x38, 0x40], np.uint8)       # 0.5 .. 2
 
 
-def _slots(counts, topk=1):
+def _slots(counts, topk=1, tight=False):
+    """Routing tables for per-expert slot counts; tight: the slot capacity ends at
+    the last expert's padded rows (no spare rows after them)."""
     counts = np.asarray(counts, np.int64)
     E = counts.size
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
@@ -47,6 +51,8 @@ def _slots(counts, topk=1):
     cap = B.moe_slot_capacity(max(T, 1), topk, E)
     cap = max(cap, int(poff[-1]))
     cap = -(-cap // 128) * 128
+    if tight:
+        cap = int(poff[-1])
     return {"counts": counts.astype(np.int32), "offsets": offs, "padded_offsets": poff}, cap
 
 
@@ -64,9 +70,9 @@ def _rand_operands(r, rows, K, exact):
     return codes, sf
 
 
-def _l1_case(counts, K, I, exact, seed, epilogue, gs=None):
+def _l1_case(counts, K, I, exact, seed, epilogue, gs=None, tight=False):
     r = np.random.default_rng(seed)
-    rt, cap = _slots(counts)
+    rt, cap = _slots(counts, tight=tight)
     E = len(counts)
     a_codes, a_sf = _rand_operands(r, cap, K, exact)        # padding rows hold garbage too
     w1c, w1s = _rand_operands(r, E * 2 * I, K, exact)
@@ -104,11 +110,23 @@ def test_l1_gateup_exact_arithmetic_bit_exact(counts, K, I):
     assert np.array_equal(got[valid, I:], u[valid])
 
 
-@pytest.mark.parametrize("counts,K,I", [([37, 200, 0, 5], 4096, 128), ([130], 1024, 256), ([3, 9], 128, 64)])
+@pytest.mark.parametrize("counts,K,I", [([37, 200, 0, 5], 4096, 128), ([130], 1024, 256), ([3, 9], 128, 64),
+                                        ([200, 61], 384, 128)])
 def test_l1_gateup_random_scales(counts, K, I):
     got, g, u, valid, _ = _l1_case(counts, K, I, False, 12, B.MOE_L1_GATEUP_BF16, gs=0.7)
     assert_layer_close(got[valid, :I], g[valid], "gate")
     assert_layer_close(got[valid, I:], u[valid], "up")
+
+
+@pytest.mark.parametrize("counts", [[100, 0, 45], [300, 129]])
+def test_l1_capacity_ends_at_last_expert(counts):
+    """Slot capacity = the last expert's padded end: a 256-row pair tile of an expert
+    with an odd number of 128-row tiles must not read past it (the peer's half is
+    empty there)."""
+    got, g, u, valid, _ = _l1_case(counts, 512, 128, True, 14, B.MOE_L1_GATEUP_BF16, tight=True)
+    assert got.shape[0] == sum(-(-c // 128) * 128 for c in counts)
+    assert np.array_equal(got[valid, :128], g[valid])
+    assert np.array_equal(got[valid, 128:], u[valid])
 
 
 def test_l1_silu_and_amax():
@@ -119,9 +137,9 @@ def test_l1_silu_and_amax():
     assert amax == np.abs(got[valid]).max()
 
 
-def _l2_case(counts, I, K, exact, seed, epilogue, gs=None, slot_token=None, slot_weight=None, T=0):
+def _l2_case(counts, I, K, exact, seed, epilogue, gs=None, slot_token=None, slot_weight=None, T=0, tight=False):
     r = np.random.default_rng(seed)
-    rt, cap = _slots(counts)
+    rt, cap = _slots(counts, tight=tight)
     E = len(counts)
     h_codes, h_sf = _rand_operands(r, cap, I, exact)
     w2c, w2s = _rand_operands(r, E * K, I, exact)
@@ -159,6 +177,12 @@ def test_l2_rows_exact_arithmetic_bit_exact(counts, I, K):
 def test_l2_rows_random_scales(counts, I, K):
     got, ref, valid, _, _ = _l2_case(counts, I, K, False, 22, B.MOE_L2_ROWS_BF16, gs=0.5)
     assert_layer_close(got[valid], ref[valid], "y")
+
+
+def test_l2_capacity_ends_at_last_expert():
+    got, ref, valid, _, _ = _l2_case([129, 5], 256, 512, True, 25, B.MOE_L2_ROWS_BF16, tight=True)
+    assert got.shape[0] == 384
+    assert np.array_equal(got[valid], ref[valid])
 
 
 def test_l2_scatter_weighted_sum():
