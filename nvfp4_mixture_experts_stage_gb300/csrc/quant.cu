@@ -13,6 +13,8 @@
 // 16-element block i and the warp's loads and code stores are fully coalesced
 // (512 B in, 128 B out).  Four consecutive block scales of a row are assembled
 // into one 32-bit store by lane 8j (they are contiguous in both scale layouts).
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -183,7 +185,121 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Block quantisation of token rows into their slots (top-k <= 8): a warp takes a run of
+// kRunSegs consecutive 256-element segments of one token row, looks the token's slots up
+// once (lane j holds slot j), precomputes each slot's code-row and scale-atom offsets,
+// and writes every segment's codes and scale words to all of them.  The arithmetic of a
+// segment is the one of quantize_kernel.
+// ---------------------------------------------------------------------------
+constexpr int kRunSegs = 4;
+
+__global__ void __launch_bounds__(256, 4) quantize_slots_kernel(QuantArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float s_rb[128];
+  if (threadIdx.x < 128) s_rb[threadIdx.x] = threadIdx.x ? __frcp_rn(e4m3_value(threadIdx.x)) : 0.0f;
+  float amax_f = 0.0f;
+  if (!a.gs_fixed) {
+    if (a.amax_partials) {
+      uint32_t m = 0;
+      for (int i = threadIdx.x & 31; i < a.n_partials; i += 32) m = max(m, __ldg(a.amax_partials + i));
+      amax_f = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, m));
+    } else {
+      amax_f = __uint_as_float(*a.amax_bits);
+    }
+  }
+  const float gs = a.gs_fixed ? __ldg(a.gs_fixed) : __fdiv_rn(amax_f, kGsDivisor);
+  const float rg = recip_global_scale(gs);
+  if (a.gs_out && blockIdx.x == 0 && threadIdx.x == 0) *a.gs_out = gs;
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const bool sf_lane = (lane & 7) == 0;
+  const uint32_t nseg = (uint32_t)((a.K + 255) >> 8);
+  const uint32_t nrun = (nseg + kRunSegs - 1) / kRunSegs;
+  const uint32_t total = (uint32_t)(a.rows * nrun);
+  const uint32_t warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const uint32_t drow = nwarps / nrun, drun = nwarps - drow * nrun;
+  uint32_t cur_row = warp0 / nrun, cur_run = warp0 - cur_row * nrun;
+  const int k_sf = a.K >> 4;
+  const int half_k = a.K >> 1;
+  const int atom_row = (k_sf >> 2) * 512;  // bytes of scale atoms per 128 slot rows
+
+  for (uint32_t t = warp0; t < total; t += nwarps) {
+    const int64_t row = cur_row;
+    const int seg0 = (int)(cur_run * kRunSegs);
+    cur_row += drow;
+    cur_run += drun;
+    if (cur_run >= nrun) { cur_run -= nrun; ++cur_row; }
+    uint4 v[kRunSegs];
+#pragma unroll
+    for (int g = 0; g < kRunSegs; ++g) {
+      const int col = (seg0 + g) * 256 + lane * 8;
+      v[g] = col < a.K ? __ldcs(a.x + row * a.ld_vec + (col >> 3)) : make_uint4(0, 0, 0, 0);
+    }
+    int32_t pj = lane < a.topk ? __ldg(a.pair_slot + row * a.topk + lane) : -1;
+    if (pj >= a.capacity) {
+      set_status(a.status, MOE_ERR_DEVICE_INDEX);
+      pj = -1;
+    }
+    // slot j's code row and scale-atom position (scale column 0); the launcher keeps
+    // capacity * K / 2 below 2^31, so 32-bit offsets hold them
+    int32_t cbase[8];
+    int32_t sbase[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int32_t p = __shfl_sync(0xFFFFFFFFu, pj, j);
+      cbase[j] = p >= 0 ? p * half_k : -1;
+      sbase[j] = (p >> 7) * atom_row + (p & 31) * 16 + ((p >> 5) & 3) * 4;
+    }
+#pragma unroll
+    for (int g = 0; g < kRunSegs; ++g) {
+      if (seg0 + g >= (int)nseg) break;  // warp-uniform
+      const uint32_t w[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(w[i]); f[2 * i + 1] = bf16hi(w[i]); }
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+      const float bm = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      const uint32_t sb = e4m3_byte(__fdiv_rn(__fmul_rn(bm, rg), 6.0f));
+      const float rb = s_rb[sb];
+      uint32_t code = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        code |= e2m1x2(__fmul_rn(__fmul_rn(f[2 * i], rg), rb), __fmul_rn(__fmul_rn(f[2 * i + 1], rg), rb)) << (8 * i);
+      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
+      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
+      const uint32_t sfw = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      const int col = (seg0 + g) * 256 + lane * 8;
+      if (col >= a.K) continue;
+      const int ks = col >> 4;
+      const int soff = (ks >> 2) * 512 + (ks & 3);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (cbase[j] < 0) continue;
+        *reinterpret_cast<uint32_t*>(a.codes + (uint32_t)(cbase[j] + (col >> 1))) = code;
+        if (sf_lane) *reinterpret_cast<uint32_t*>(a.sf + (uint32_t)(sbase[j] + soff)) = sfw;
+      }
+    }
+  }
+}
+
 cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st, bool pdl) {
+  if (dst == kDstSlots && a.topk <= 8 && a.capacity * (int64_t)(a.K / 2) < (int64_t(1) << 31)) {
+    // tasks of kRunSegs segments; four 256-thread blocks fit per SM
+    const int64_t tasks = a.rows * (int64_t)(((a.K + 255) / 256 + kRunSegs - 1) / kRunSegs);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int b = (int)std::min<int64_t>(std::max<int64_t>((tasks + 7) / 8, 1), (int64_t)sms * 4);
+    (void)blocks;
+    return launch_ex(quantize_slots_kernel, b, 256, 0, st, pdl, a);
+  }
   switch (dst) {
     case kDstRowMajorSf: return launch_ex(quantize_kernel<kDstRowMajorSf>, blocks, 256, 0, st, pdl, a);
     case kDstSwizzledSf: return launch_ex(quantize_kernel<kDstSwizzledSf>, blocks, 256, 0, st, pdl, a);

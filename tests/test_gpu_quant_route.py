@@ -147,9 +147,18 @@ def test_route_no_local_experts():
     assert got["offsets"][-1] == 0 and np.all(got["pair_slot"] == -1)
 
 
-def test_stage_to_slots_bit_exact():
-    wl = workloads.small("slots", T=300, K=512, I=64, E=5, topk=3)
+@pytest.mark.parametrize("T,K,topk,E,nonlocal_", [(300, 512, 3, 5, False), (77, 320, 8, 10, False),
+                                                  (64, 4096, 8, 48, True), (50, 256, 9, 12, False),
+                                                  (129, 1152, 2, 4, True)])
+def test_stage_to_slots_bit_exact(T, K, topk, E, nonlocal_):
+    """Every slot holds its token's codes and scales: runs of segments ending inside a
+    row (K = 320, 1152), top-8, top-9 (the general kernel), pairs of other ranks' experts
+    (no slot)."""
+    wl = workloads.small("slots", T=T, K=K, I=64, E=E, topk=topk)
     ids, w = workloads.routing(wl)
+    if nonlocal_:
+        ids = ids.copy()
+        ids[::3] += E          # every third pair belongs to another rank
     x = workloads.activations(wl)
     rt = oroute(ids, w, wl.E, 0)
     cap = B.moe_slot_capacity(wl.T, wl.topk, wl.E)
@@ -161,11 +170,16 @@ def test_stage_to_slots_bit_exact():
                                     ws=ws)
     torch.cuda.synchronize()
     rc, rs, rg = q.quantize(x.float().numpy())
-    valid = rt["slot_token"] >= 0
+    # the oracle's slot table ends at the last expert's padded end; rows after it stay zero
+    slot_token = np.full(cap, -1, np.int64)
+    slot_token[:len(rt["slot_token"])] = rt["slot_token"]
+    valid = slot_token >= 0
     assert np.float32(gs.item()) == rg
-    assert np.array_equal(a.cpu().numpy()[valid], rc[rt["slot_token"][valid]])
+    got = a.cpu().numpy()
+    assert np.array_equal(got[valid], rc[slot_token[valid]])
+    assert not got[len(rt["slot_token"]):].any()
     got_sf = q.unswizzle(asf.cpu().numpy(), cap, wl.K // 16)
-    assert np.array_equal(got_sf[valid], rs[rt["slot_token"][valid]])
+    assert np.array_equal(got_sf[valid], rs[slot_token[valid]])
 
 
 def test_prepare_weights_layout():
