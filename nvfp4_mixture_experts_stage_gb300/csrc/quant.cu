@@ -187,12 +187,14 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
 
 // ---------------------------------------------------------------------------
 // Block quantisation of token rows into their slots (top-k <= 8): a warp takes a run of
-// kRunSegs consecutive 256-element segments of one token row, looks the token's slots up
-// once (lane j holds slot j), precomputes each slot's code-row and scale-atom offsets,
-// and writes every segment's codes and scale words to all of them.  The arithmetic of a
-// segment is the one of quantize_kernel.
+// 1024 consecutive elements of one token row; lane l holds elements [32l, 32l+32) (two
+// whole 16-element blocks, so no block maximum crosses lanes) and writes their 16 code
+// bytes with one 16-byte store per slot; lanes 2m and 2m+1 together hold the four block
+// scales of one scale word, which lane 2m stores.  The token's slots are looked up once
+// per run (lane j holds slot j) with each slot's code-row and scale-atom offsets.  The
+// arithmetic of every element is the one of quantize_kernel.
 // ---------------------------------------------------------------------------
-constexpr int kRunSegs = 4;
+constexpr int kRunElems = 1024;
 
 __global__ void __launch_bounds__(256, 4) quantize_slots_kernel(QuantArgs a) {
   griddep_wait();
@@ -215,9 +217,7 @@ __global__ void __launch_bounds__(256, 4) quantize_slots_kernel(QuantArgs a) {
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
-  const bool sf_lane = (lane & 7) == 0;
-  const uint32_t nseg = (uint32_t)((a.K + 255) >> 8);
-  const uint32_t nrun = (nseg + kRunSegs - 1) / kRunSegs;
+  const uint32_t nrun = (uint32_t)((a.K + kRunElems - 1) / kRunElems);
   const uint32_t total = (uint32_t)(a.rows * nrun);
   const uint32_t warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -229,16 +229,16 @@ __global__ void __launch_bounds__(256, 4) quantize_slots_kernel(QuantArgs a) {
 
   for (uint32_t t = warp0; t < total; t += nwarps) {
     const int64_t row = cur_row;
-    const int seg0 = (int)(cur_run * kRunSegs);
+    const int col = (int)cur_run * kRunElems + lane * 32;  // first element of this lane
     cur_row += drow;
     cur_run += drun;
     if (cur_run >= nrun) { cur_run -= nrun; ++cur_row; }
-    uint4 v[kRunSegs];
+    // K is a multiple of 64, so a lane's 32 elements are all inside the row or all past it
+    const bool in = col < a.K;
+    uint4 v[4];
 #pragma unroll
-    for (int g = 0; g < kRunSegs; ++g) {
-      const int col = (seg0 + g) * 256 + lane * 8;
-      v[g] = col < a.K ? __ldcs(a.x + row * a.ld_vec + (col >> 3)) : make_uint4(0, 0, 0, 0);
-    }
+    for (int i = 0; i < 4; ++i)
+      v[i] = in ? __ldcs(a.x + row * a.ld_vec + (col >> 3) + i) : make_uint4(0, 0, 0, 0);
     int32_t pj = lane < a.topk ? __ldg(a.pair_slot + row * a.topk + lane) : -1;
     if (pj >= a.capacity) {
       set_status(a.status, MOE_ERR_DEVICE_INDEX);
@@ -254,45 +254,55 @@ __global__ void __launch_bounds__(256, 4) quantize_slots_kernel(QuantArgs a) {
       cbase[j] = p >= 0 ? p * half_k : -1;
       sbase[j] = (p >> 7) * atom_row + (p & 31) * 16 + ((p >> 5) & 3) * 4;
     }
+    // two blocks of 16: codes and scale bytes
+    uint32_t code[4];
+    uint32_t sb2 = 0;
 #pragma unroll
-    for (int g = 0; g < kRunSegs; ++g) {
-      if (seg0 + g >= (int)nseg) break;  // warp-uniform
-      const uint32_t w[4] = {v[g].x, v[g].y, v[g].z, v[g].w};
-      float f[8];
+    for (int b = 0; b < 2; ++b) {
+      float f[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(w[i]); f[2 * i + 1] = bf16hi(w[i]); }
-      float m = 0.0f;
+      for (int i = 0; i < 2; ++i) {
+        const uint4 q = v[2 * b + i];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-      const float bm = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        for (int k = 0; k < 4; ++k) { f[8 * i + 2 * k] = bf16lo(w[k]); f[8 * i + 2 * k + 1] = bf16hi(w[k]); }
+      }
+      float bm = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) bm = fmaxf(bm, fabsf(f[i]));
       const uint32_t sb = e4m3_byte(__fdiv_rn(__fmul_rn(bm, rg), 6.0f));
       const float rb = s_rb[sb];
-      uint32_t code = 0;
+      sb2 |= sb << (8 * b);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        code |= e2m1x2(__fmul_rn(__fmul_rn(f[2 * i], rg), rb), __fmul_rn(__fmul_rn(f[2 * i + 1], rg), rb)) << (8 * i);
-      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
-      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
-      const uint32_t sfw = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      const int col = (seg0 + g) * 256 + lane * 8;
-      if (col >= a.K) continue;
-      const int ks = col >> 4;
-      const int soff = (ks >> 2) * 512 + (ks & 3);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t c = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (cbase[j] < 0) continue;
-        *reinterpret_cast<uint32_t*>(a.codes + (uint32_t)(cbase[j] + (col >> 1))) = code;
-        if (sf_lane) *reinterpret_cast<uint32_t*>(a.sf + (uint32_t)(sbase[j] + soff)) = sfw;
+        for (int i = 0; i < 4; ++i)
+          c |= e2m1x2(__fmul_rn(__fmul_rn(f[8 * h + 2 * i], rg), rb), __fmul_rn(__fmul_rn(f[8 * h + 2 * i + 1], rg), rb))
+               << (8 * i);
+        code[2 * b + h] = c;
       }
+    }
+    // scale word of blocks 4m..4m+3 on lane 2m: its two bytes, then lane 2m+1's two
+    const uint32_t sfw = sb2 | (__shfl_down_sync(0xFFFFFFFFu, sb2, 1) << 16);
+    if (!in) continue;
+    const bool sf_lane = (lane & 1) == 0;
+    const int ks = col >> 4;  // scale column of this lane's first block (a multiple of 4 on sf lanes)
+    const int soff = (ks >> 2) * 512;
+    const uint4 cw = make_uint4(code[0], code[1], code[2], code[3]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (cbase[j] < 0) continue;
+      *reinterpret_cast<uint4*>(a.codes + (uint32_t)(cbase[j] + (col >> 1))) = cw;
+      if (sf_lane) *reinterpret_cast<uint32_t*>(a.sf + (uint32_t)(sbase[j] + soff)) = sfw;
     }
   }
 }
 
 cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st, bool pdl) {
   if (dst == kDstSlots && a.topk <= 8 && a.capacity * (int64_t)(a.K / 2) < (int64_t(1) << 31)) {
-    // tasks of kRunSegs segments; four 256-thread blocks fit per SM
-    const int64_t tasks = a.rows * (int64_t)(((a.K + 255) / 256 + kRunSegs - 1) / kRunSegs);
+    // tasks of kRunElems elements; four 256-thread blocks fit per SM
+    const int64_t tasks = a.rows * (int64_t)((a.K + kRunElems - 1) / kRunElems);
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
