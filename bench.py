@@ -512,6 +512,9 @@ def sweep_configs(pk, B, reps=20):
         sws = torch.empty(B.moe_stage_workspace_size(), dtype=torch.uint8, device="cuda")
 
         def timed(fn):
+            """Device time per call: `reps` calls captured in one CUDA graph, replayed;
+            also the time per call issued eagerly from Python (host-bound for small
+            calls)."""
             for i in range(3):
                 fn(i)
             torch.cuda.synchronize()
@@ -521,9 +524,27 @@ def sweep_configs(pk, B, reps=20):
                 fn(i)
             e1.record()
             torch.cuda.synchronize()
-            return e0.elapsed_time(e1) / reps
+            eager = e0.elapsed_time(e1) / reps
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    for i in range(reps):
+                        fn(i)
+            torch.cuda.current_stream().wait_stream(side)
+            g.replay()
+            torch.cuda.synchronize()
+            n = 5
+            e0.record()
+            for _ in range(n):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / (n * reps), eager
 
-        q_ms = timed(lambda i: B.moe_stage_activation(xs[i % nbuf], codes, sf, B.MOE_SF_SWIZZLED, gs, ws=sws))
+        q_ms, q_eager = timed(lambda i: B.moe_stage_activation(xs[i % nbuf], codes, sf, B.MOE_SF_SWIZZLED, gs,
+                                                                ws=sws))
         q_bytes = xbytes * (2 if xbytes > L2_BYTES else 1) + T * K // 2 + T * K // 16
         ids_np, w_np = workloads.routing(wl)
         ids, w = torch.from_numpy(ids_np).cuda(), torch.from_numpy(w_np).cuda()
@@ -534,18 +555,20 @@ def sweep_configs(pk, B, reps=20):
                     slot_weight=torch.empty(cap, dtype=torch.float32, device="cuda"),
                     pair_slot=torch.empty(T * topk, **i32))
         rws = torch.empty(B.moe_route_workspace_size(T, topk, E), dtype=torch.uint8, device="cuda")
-        r_ms = timed(lambda i: B.moe_route(ids, w, E, wl.expert_offset, rbuf["counts"], rbuf["offsets"],
-                                          rbuf["padded_offsets"], rbuf["slot_token"], rbuf["slot_weight"],
-                                          rbuf["pair_slot"], rws))
+        r_ms, r_eager = timed(lambda i: B.moe_route(ids, w, E, wl.expert_offset, rbuf["counts"], rbuf["offsets"],
+                                                    rbuf["padded_offsets"], rbuf["slot_token"], rbuf["slot_weight"],
+                                                    rbuf["pair_slot"], rws))
         r_bytes = T * topk * 20
         q_gbs, r_gbs = q_bytes / (q_ms * 1e-3) / 1e9, r_bytes / (r_ms * 1e-3) / 1e9
         out[name] = {
             "workload": f"{wl.name}: T={T}, K={K}, E={E}, top-{topk} (stage_activation and routing alone)",
-            "stage_activation": {"us": q_ms * 1e3, "algorithmic_bytes": q_bytes,
+            "timing": f"device time per call: {reps} calls in one CUDA graph, replayed; us_eager = issued "
+                      "one by one from Python",
+            "stage_activation": {"us": q_ms * 1e3, "us_eager": q_eager * 1e3, "algorithmic_bytes": q_bytes,
                                  "roofline": {"bound": "hbm", "achieved": q_gbs, "peak": pk["hbm_gbs"],
                                               "unit": "GB/s", "frac": q_gbs / pk["hbm_gbs"],
                                               "peak_source": pk["source"]}},
-            "route": {"us": r_ms * 1e3, "algorithmic_bytes": r_bytes,
+            "route": {"us": r_ms * 1e3, "us_eager": r_eager * 1e3, "algorithmic_bytes": r_bytes,
                       "roofline": {"bound": "hbm", "achieved": r_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                    "frac": r_gbs / pk["hbm_gbs"], "peak_source": pk["source"]}},
         }

@@ -57,17 +57,28 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = warp; e < E; e += 32) {
     int running = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < nchunks ? cnt[(int64_t)e * nchunks + c] : 0;
-      int incl = v;
+    const int32_t* row = cnt + (int64_t)e * nchunks;
+    int32_t* brow = base + (int64_t)e * nchunks;
+    // 256 chunks per round: their counts are loaded together, then scanned 32 at a time
+    for (int c0 = 0; c0 < nchunks; c0 += 256) {
+      int v[8];
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += t;
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + 32 * i + lane;
+        v[i] = c < nchunks ? __ldcg(row + c) : 0;
       }
-      if (c < nchunks) base[(int64_t)e * nchunks + c] = running + incl - v;
-      running += __shfl_sync(0xFFFFFFFFu, incl, 31);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        int incl = v[i];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+          if (lane >= d) incl += t;
+        }
+        const int c = c0 + 32 * i + lane;
+        if (c < nchunks) brow[c] = running + incl - v[i];
+        running += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
     }
     if (lane == 0) s_cnt[e] = running;
   }
@@ -114,10 +125,19 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_place_kernel(
   __syncwarp();
   const int64_t base_idx = (int64_t)chunk * kRouteChunk;
   const unsigned lower = (1u << lane) - 1u;
-#pragma unroll 2
+  // the chunk's experts and weights, loaded together
+  int loc[kRouteChunk / 32];
+  float wt[kRouteChunk / 32];
+#pragma unroll
   for (int g = 0; g < kRouteChunk / 32; ++g) {
     const int64_t idx = base_idx + g * 32 + lane;
-    const int l = local_expert(ids, idx, P, off, E);
+    loc[g] = local_expert(ids, idx, P, off, E);
+    wt[g] = idx < P ? __ldg(w + idx) : 0.0f;
+  }
+#pragma unroll
+  for (int g = 0; g < kRouteChunk / 32; ++g) {
+    const int64_t idx = base_idx + g * 32 + lane;
+    const int l = loc[g];
     const unsigned grp = __match_any_sync(0xFFFFFFFFu, l);
     int slot = -1;
     if (l >= 0) slot = run[warp][l] + __popc(grp & lower);
@@ -132,7 +152,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_place_kernel(
       pair_slot[idx] = slot;
       if (slot >= 0) {
         slot_token[slot] = (int32_t)(idx / topk);
-        slot_weight[slot] = __ldg(w + idx);
+        slot_weight[slot] = wt[g];
       }
     }
   }
@@ -325,7 +345,10 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk
                          int32_t* base, int nchunks, int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
                          int32_t* slot_token, float* slot_weight, int32_t* pair_slot, int64_t capacity,
                          int32_t* status, cudaStream_t st) {
-  if (P <= kSmallRoutePairs) {
+  // one block up to 4096 pairs: above that its scattered slot stores (all from one SM)
+  // take longer than the three launches of the chunked path (8192 pairs: 20 us against
+  // ~12 us); the layer's fused prologue still routes up to 8192 pairs in its block 0
+  if (P <= kSmallRoutePairs / 2) {
     static bool configured = false;
     const int smem = 32 * kMaxExperts * (int)sizeof(int);
     if (!configured) {

@@ -132,6 +132,16 @@ def test_route_bit_exact_random_with_invalid_ids(seed):
     _check_route(ids, w, E, off)
 
 
+@pytest.mark.parametrize("P", [4096, 4097, 8192, 8193])
+def test_route_bit_exact_at_path_boundaries(P):
+    """Pair counts around the switch from the one-block kernel to the chunked kernels."""
+    r = np.random.default_rng(P)
+    k, E = 1, 48
+    ids = r.integers(0, E + 8, (P, k)).astype(np.int32)   # some pairs belong to other ranks
+    w = r.random((P, k)).astype(np.float32)
+    _check_route(ids, w, E, 0)
+
+
 def test_route_identity_for_sorted_top1():
     wl = workloads.WORKLOADS["skew_top1"]
     ids, w = workloads.routing(wl)
