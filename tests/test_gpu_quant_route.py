@@ -71,6 +71,55 @@ def test_stage_activation_fixed_scale_bit_exact(gs_fixed):
     assert np.array_equal(sf.reshape(48, 16), rs)
 
 
+def _finite_bf16():
+    f = q.bf16_from_bits(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    return f[np.isfinite(f)]
+
+
+def _blocks_to_rows(blocks):
+    """[n, 16] blocks -> rows of K = 256 (zero blocks pad the last row)."""
+    n = -(-len(blocks) // 16) * 16
+    out = np.zeros((n, 16), np.float32)
+    out[:len(blocks)] = blocks
+    return out.reshape(-1, 256)
+
+
+@pytest.mark.parametrize("bm", [6.0, 3.0, 0.375])
+def test_every_bf16_value_codes_bit_exact(bm):
+    """The E2M1 encoder on every finite BF16 value v with |v| <= bm, both signs and -0:
+    each block holds bm and 15 such values, so with gs = 1 the block scale is bm/6 (an
+    exact e4m3 value: 1, 0.5, 0.0625) and every code is the encoder's rounding of v*6/bm."""
+    f = _finite_bf16()
+    v = f[np.abs(f) <= bm]
+    n = -(-len(v) // 15)
+    vals = np.zeros(n * 15, np.float32)
+    vals[:len(v)] = v
+    blocks = np.concatenate([np.full((n, 1), bm, np.float32), vals.reshape(n, 15)], axis=1)
+    x = _blocks_to_rows(blocks)
+    codes, sf, _ = _stage(x, 0, 1.0)
+    rc, rs, _ = q.quantize(x, np.float32(1.0))
+    assert np.array_equal(codes, rc)
+    assert np.array_equal(sf.reshape(rs.shape), rs)
+
+
+@pytest.mark.parametrize("gs_fixed", [1.0, 1.0 / 3.0])
+def test_every_bf16_block_max_scale_bit_exact(gs_fixed):
+    """The E4M3 scale encoder on every positive finite BF16 block maximum bm (zero,
+    subnormal, normal and saturating scales bm*rg/6), with the block's other values
+    -bm, bm/2 and zeros."""
+    f = _finite_bf16()
+    bms = f[f > 0]
+    blocks = np.zeros((len(bms), 16), np.float32)
+    blocks[:, 0] = bms
+    blocks[:, 1] = -bms
+    blocks[:, 2] = q.bf16_round(bms / 2)
+    x = _blocks_to_rows(blocks)
+    codes, sf, _ = _stage(x, 0, gs_fixed)
+    rc, rs, _ = q.quantize(x, np.float32(gs_fixed))
+    assert np.array_equal(sf.reshape(rs.shape), rs)
+    assert np.array_equal(codes, rc)
+
+
 def test_stage_activation_ties_signs_and_golden_blocks():
     # every E2M1 tie and grid point, both signs, with scale 1 (block max 6, gs 1)
     vals = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0],
