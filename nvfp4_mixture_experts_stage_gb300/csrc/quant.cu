@@ -303,9 +303,12 @@ cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_
   if (dst == kDstSlots && a.topk <= 8 && a.capacity * (int64_t)(a.K / 2) < (int64_t(1) << 31)) {
     // tasks of kRunElems elements; four 256-thread blocks fit per SM
     const int64_t tasks = a.rows * (int64_t)((a.K + kRunElems - 1) / kRunElems);
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static int sms = 0;
+    if (!sms) {
+      int dev = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
     const int b = (int)std::min<int64_t>(std::max<int64_t>((tasks + 7) / 8, 1), (int64_t)sms * 4);
     (void)blocks;
     return launch_ex(quantize_slots_kernel, b, 256, 0, st, pdl, a);
