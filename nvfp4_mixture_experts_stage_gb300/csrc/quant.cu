@@ -300,7 +300,10 @@ __global__ void __launch_bounds__(256, 4) quantize_slots_kernel(QuantArgs a) {
 }
 
 cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st, bool pdl) {
-  if (dst == kDstSlots && a.topk <= 8 && a.capacity * (int64_t)(a.K / 2) < (int64_t(1) << 31)) {
+  // the run kernel stores 16 code bytes at a time: it needs a 16-byte aligned code buffer
+  // (the API asks for 4); 32-bit offsets need capacity * K / 2 < 2^31
+  if (dst == kDstSlots && a.topk <= 8 && a.capacity * (int64_t)(a.K / 2) < (int64_t(1) << 31) &&
+      (reinterpret_cast<uintptr_t>(a.codes) & 15) == 0) {
     // tasks of kRunElems elements; four 256-thread blocks fit per SM
     const int64_t tasks = a.rows * (int64_t)((a.K + kRunElems - 1) / kRunElems);
     static int sms = 0;
