@@ -355,6 +355,18 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E,
                               void* ws, size_t ws_bytes, void* const* stage_events,
                               moe_stream_t stream);
 
+/* Self-test of the failure reporting the kernels rely on (no counterpart on the commit
+ * pages).  Launches one block on `stream` in which thread 0 waits, with the library's
+ * bounded mbarrier wait, on a barrier that nothing arrives on, and thread 32 waits on a
+ * second such barrier starting half a limit later.  Thread 0 gives up after the wait
+ * limit (1 s), sets the block's abort flag and writes MOE_ERR_TIMEOUT to *dev_status
+ * (first error wins); thread 32 must then return through the abort flag before its own
+ * limit.  dev_result (2 int32, device): [0] = 1 if thread 0 gave up on its limit,
+ * [1] = 1 if thread 32 returned through the abort flag.  Nothing waits forever and the
+ * context stays usable.  Returns MOE_ERR_INVALID_ARG for NULL pointers, MOE_ERR_CUDA if
+ * the launch fails; takes about one second of device time. */
+moe_status moe_selftest_bounded_wait(int32_t* dev_status, int32_t* dev_result, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

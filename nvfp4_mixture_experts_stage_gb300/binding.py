@@ -37,7 +37,7 @@ EXPORTS = (
     "moe_stage_activation", "moe_stage_activation_to_slots", "moe_route",
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
     "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
-    "moe_set_gemm_policy", "moe_combine_rows",
+    "moe_set_gemm_policy", "moe_combine_rows", "moe_selftest_bounded_wait",
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
@@ -82,6 +82,7 @@ def _load():
         "moe_grouped_gemm_l2": (I32, [P, P, P, P, P, I32, I64, I32, I32, P, P, P, I32, P, P, P, P, I64, P, P]),
         "moe_cast_output": (I32, [P, P, I64, I32, P]),
         "moe_combine_rows": (I32, [P, I64, P, P, I64, I32, I32, I64, P, P, P]),
+        "moe_selftest_bounded_wait": (I32, [P, P, P]),
         "moe_set_gemm_policy": (I32, [I32]),
         "moe_forward": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32, P, P,
                               P, P, SZ, P]),
@@ -222,6 +223,13 @@ def moe_grouped_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, I, K, w2_
 def moe_cast_output(out32, out_bf16, stream=None):
     T, K = out32.shape
     _check("moe_cast_output", _lib.moe_cast_output(_p(out32), _p(out_bf16), T, K, _stream(stream)))
+
+
+def moe_selftest_bounded_wait(dev_status, dev_result, stream=None):
+    """Failure-reporting self-test (see include/moe_stage.h): about one second of device
+    time; afterwards dev_status holds MOE_ERR_TIMEOUT and dev_result (2 int32) [1, 1]."""
+    _check("moe_selftest_bounded_wait", _lib.moe_selftest_bounded_wait(_p(dev_status), _p(dev_result),
+                                                                       _stream(stream)))
 
 
 def moe_combine_rows(y_rows, pair_slot, topk_w, out_bf16, capacity=None, dev_status=None, stream=None):

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(LIBDIR, "libmoe_stage.so")
-SOURCES = ["api.cu", "quant.cu", "route.cu", "gemm.cu", "gemm_pair.cu", "route_static.cu", "gemm_stream.cu"]
+SOURCES = ["api.cu", "quant.cu", "route.cu", "gemm.cu", "gemm_pair.cu", "route_static.cu", "gemm_stream.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -143,6 +143,11 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
+moe_status moe_selftest_bounded_wait(int32_t* dev_status, int32_t* dev_result, moe_stream_t stream) {
+  if (!dev_status || !dev_result) return MOE_ERR_INVALID_ARG;
+  return selftest_bounded_wait(dev_status, dev_result, (cudaStream_t)stream);
+}
+
 int moe_set_gemm_policy(int policy) {
   if (policy < MOE_GEMM_AUTO || policy > MOE_GEMM_TILED_PAIR) return -1;
   return set_gemm_policy(policy);

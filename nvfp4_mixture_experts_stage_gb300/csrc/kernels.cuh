@@ -106,6 +106,9 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
                                  void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
                                  int64_t T, int32_t* status, cudaStream_t st, bool pdl = false);
 
+// Bounded-wait self-test (selftest.cu).
+moe_status selftest_bounded_wait(int32_t* status, int32_t* result, cudaStream_t st);
+
 // Which grouped-GEMM kernel runs (process-wide; moe_set_gemm_policy).
 int gemm_policy();
 int set_gemm_policy(int policy);

@@ -86,6 +86,7 @@ def test_argument_checks_fail_before_any_device_work(B):
     assert lib.moe_grouped_gemm_l1(null, null, null, null, null, 1, 128, 256, 128, null, null, null, null, 0,
                                    null, null, null, null, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_cast_output(null, null, 4, 7, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_bounded_wait(null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_combine_rows(null, 8, null, null, 4, 2, 7, 16, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_combine_rows(null, 8, null, null, 4, 2, 8, 16, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_combine_rows(null, 8, null, null, 0, 2, 8, 16, null, null, null) == B.MOE_OK  # nothing to do

@@ -164,3 +164,28 @@ def test_stage_to_slots_code_buffer_aligned_to_4_bytes_only():
     rc, _, _ = q.quantize(x)
     for i in range(T * topk):
         assert np.array_equal(outs[1][0][ps[i]], rc[i // topk])
+
+
+def test_bounded_wait_gives_up_reports_timeout_and_leaves_the_context_usable():
+    """A wait on a barrier nothing completes ends after the library's limit with
+    MOE_ERR_TIMEOUT; a second waiter returns through the abort flag; the next call works."""
+    import time
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = torch.zeros(2, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    B.moe_selftest_bounded_wait(st, res)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert st.item() == B.MOE_ERR_TIMEOUT
+    assert res.cpu().tolist() == [1, 1]
+    assert 0.9 < dt < 10.0
+    # the context still runs work
+    x = q.bf16_round(np.random.default_rng(9).standard_normal((4, 64)).astype(np.float32))
+    codes = torch.zeros(4, 32, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(4 * 4, dtype=torch.uint8, device="cuda")
+    gs = torch.zeros(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.moe_stage_workspace_size(), dtype=torch.uint8, device="cuda")
+    B.moe_stage_activation(torch.from_numpy(x).to(torch.bfloat16).cuda(), codes, sf, B.MOE_SF_ROWMAJOR, gs, ws=ws)
+    torch.cuda.synchronize()
+    rc, rs, rg = q.quantize(x)
+    assert np.array_equal(codes.cpu().numpy(), rc) and np.float32(gs.item()) == rg
