@@ -109,17 +109,20 @@ class Forward:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.wstruct = layer.weights_struct()
 
-    def __call__(self, x, topk_ids, topk_w, gs_x_fixed=None, stream=None, events=None):
+    def __call__(self, x, topk_ids, topk_w, gs_x_fixed=None, stream=None, events=None, out=None):
+        """The layer on x; writes `out` ([T, K] BF16 on the device) if given, else the
+        object's own output buffer, and returns it."""
         L = self.layer
+        o = self.out if out is None else out
         if events is None:
             B.moe_forward(x, topk_ids, topk_w, L.E, L.I, L.expert_offset, self.wstruct, self.gs_h_mode,
-                          self.gs_h, self.out, self.ws, gs_x_fixed=gs_x_fixed, dev_status=self.status,
+                          self.gs_h, o, self.ws, gs_x_fixed=gs_x_fixed, dev_status=self.status,
                           stream=stream)
         else:
             B.moe_forward_traced(x, topk_ids, topk_w, L.E, L.I, L.expert_offset, self.wstruct, self.gs_h_mode,
-                                 self.gs_h, self.out, self.ws, events, gs_x_fixed=gs_x_fixed,
+                                 self.gs_h, o, self.ws, events, gs_x_fixed=gs_x_fixed,
                                  dev_status=self.status, stream=stream)
-        return self.out
+        return o
 
 
 def run_forward(layer, x, topk_ids, topk_w, gs_h_mode=B.MOE_GS_DYNAMIC, gs_h=None, gs_x_fixed=None):
