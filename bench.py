@@ -38,7 +38,7 @@ METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture
 # (profiles/gemm_l1_stream_decode.md), valid only for the GEMM sources it was taken on.
-NCU_TRAFFIC = {"gemm_l1": {"bytes": 673970176, "sources_sha256_16": "6759e86ca63c889e"}}
+NCU_TRAFFIC = {"gemm_l1": {"bytes": 673994496, "sources_sha256_16": "386461e8bd4443fd"}}
 
 
 def gemm_sources_hash():
