@@ -172,7 +172,10 @@ def build_layer(wl, R):
 
 
 def algorithmic(wl, counts):
-    """Bytes and flops the layer must move / do for this routing (real slots only)."""
+    """Bytes and flops the layer must move / do for this routing (real slots only): the
+    touched experts' weights, the activations and h in NVFP4 once each, and the BF16
+    output once (per-slot output rows or an fp32 accumulator are this implementation's
+    choices, not the method's)."""
     K, I = wl.K, wl.I
     S = int(counts.sum())
     touched = int((counts > 0).sum())
@@ -181,7 +184,7 @@ def algorithmic(wl, counts):
     a = S * (K // 2 + K // 16)
     h = S * (I // 2 + I // 16)
     l1_bytes = w1 + a + h
-    l2_bytes = w2 + h + S * K * 4          # fp32 scatter into the output rows
+    l2_bytes = w2 + h + wl.T * K * 2       # the layer's BF16 output (the weighted scatter's result)
     flops_l1 = 2 * S * K * 2 * I
     flops_l2 = 2 * S * I * K
     return {"S": S, "touched": touched, "l1_bytes": l1_bytes, "l2_bytes": l2_bytes,
