@@ -38,14 +38,14 @@ METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture
 # (profiles/gemm_l1_stream_decode.md), valid only for the GEMM sources it was taken on.
-NCU_TRAFFIC = {"gemm_l1": {"bytes": 673994496, "sources_sha256_16": "386461e8bd4443fd"}}
+NCU_TRAFFIC = {"gemm_l1": {"bytes": 673994496, "sources_sha256_16": "c90dac2ab5142603"}}
 
 
 def gemm_sources_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm_pair.cu", "gemm_tiled.cuh", "gemm_stream.cu", "tcgen05.cuh", "kernels.cuh",
-              "common.cuh"):
+    # the files holding the grouped-GEMM kernels' code (kernels.cuh only declares launchers)
+    for f in ("gemm.cu", "gemm_pair.cu", "gemm_tiled.cuh", "gemm_stream.cu", "tcgen05.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_stage_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -166,7 +166,7 @@ def build_layer(wl, R):
     with cf.ThreadPoolExecutor(8) as ex:
         w1 = list(ex.map(lambda e: workloads.expert_w1(wl, e), range(wl.E)))
         w2 = list(ex.map(lambda e: workloads.expert_w2(wl, e), range(wl.E)))
-    layer = R.quantize_weights_on_device(wl, lambda e: w1[e], lambda e: w2[e])
+    layer = R.quantize_weights_on_device(wl, lambda e: w1[e], lambda e: w2[e], keep_rowmajor=True)
     del w1, w2
     return layer
 
@@ -472,6 +472,7 @@ def run_ours(args, ws, rank, local):
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["accuracy"] = accuracy_vs_bf16(wl, fw, x, ids, w, x_c, ids_np, w_np)
+        result["weight_study"] = weight_study(wl, layer, fw, x, ids, w, x_c, ids_np, w_np, B, R)
     if not args.no_configs:
         result["configs"] = other_configs(wl, layer, fp4_peak, pk, flush, ws, R, B)
         result["configs"].update(sweep_configs(pk, B))
@@ -499,6 +500,104 @@ def accuracy_vs_bf16(wl, fw, x, ids, w, x_c, ids_np, w_np, n_tokens=24):
     cos = float((got[live] * ref[live]).sum() / np.sqrt((got[live] ** 2).sum() * (ref[live] ** 2).sum()))
     return {"cosine_vs_bf16": cos, "tokens": int(live.sum()),
             "reference": "oracle forward_bf16 (no NVFP4 quantisation, same BF16 rounding points)"}
+
+
+def weight_study(wl, layer, fw, x, ids, w, x_c, ids_np, w_np, B, R, n_tokens=16):
+    """The pages' weight-path accuracy comparison on synthetic weights (not timed).
+    Reference: the BF16 layer (oracle forward_bf16) on the layer's NVFP4 weights
+    dequantised to BF16 -- the "checkpoint" as the pages' layertest sees it.  Against it:
+    direct (the NVFP4 weights used as they are: two alphas for gate and up), fold (the
+    pages' one-alpha form: the ratio of the two W1 global scales folded into the smaller
+    half's block scales, moe_fold_gate_up_scales), double (the dequantised BF16 weights
+    quantised again, the layertest path the pages found ~1 % cosine worse).  The same
+    call as the timed one (fixed h scale) on the whole batch; cosine on the first
+    n_tokens tokens that reach a local expert."""
+    from oracle import moe as omoe
+    E, I, K = wl.E, wl.I, wl.K
+    tokens = np.arange(min(n_tokens, wl.T))
+    loc = ids_np[tokens].reshape(-1).astype(np.int64) - wl.expert_offset
+    touched = sorted(set(int(l) for l in loc if 0 <= l < E))
+    lut = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0],
+                       device="cuda")
+
+    def dq(codes, sf, gs):
+        """E2M1 value x UE4M3 scale x global scale (fp32 product) rounded to BF16."""
+        v = torch.stack([lut[(codes & 15).long()], lut[(codes >> 4).long()]], -1).reshape(codes.shape[0], -1)
+        return (v * sf.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=1) * gs).to(torch.bfloat16)
+
+    dq_w1 = {e: torch.cat([dq(layer.w1_fp4[e, :I], layer.w1_sf_rowmajor[e, :I], layer.gs_w1_gate[e]),
+                           dq(layer.w1_fp4[e, I:], layer.w1_sf_rowmajor[e, I:], layer.gs_w1_up[e])]) for e in touched}
+    dq_w2 = {e: dq(layer.w2_fp4[e], layer.w2_sf_rowmajor[e], layer.gs_w2[e]) for e in touched}
+    ref = omoe.forward_bf16(x_c.float().numpy(), ids_np, w_np, E, wl.expert_offset,
+                            lambda e: dq_w1[e].float().cpu().numpy(), lambda e: dq_w2[e].float().cpu().numpy(),
+                            tokens=tokens)
+    live = np.abs(ref).sum(axis=1) > 0
+
+    def run(lay):
+        f = R.Forward(lay, wl.T, fw.gs_h_mode)
+        f.gs_h.copy_(fw.gs_h)
+        out = f(x, ids, w).float().cpu().numpy()[tokens]
+        if int(f.status.item()) != 0:
+            raise RuntimeError(f"weight study: device status {int(f.status.item())}")
+        a, b = out[live].astype(np.float64), ref[live].astype(np.float64)
+        return float((a * b).sum() / np.sqrt((a * a).sum() * (b * b).sum()))
+
+    def variant(w1_fp4, w1_sfr, gg, gu, w2_fp4, w2_sfr, g2):
+        return R._prepare(R.Layer(K=K, I=I, E=E, topk=layer.topk, expert_offset=layer.expert_offset,
+                                  w1_fp4=w1_fp4, w1_sf=None, gs_w1_gate=gg, gs_w1_up=gu, w2_fp4=w2_fp4, w2_sf=None,
+                                  gs_w2=g2, w1_sf_rowmajor=w1_sfr, w2_sf_rowmajor=w2_sfr))
+
+    direct = run(layer)
+    # fold: one alpha per expert
+    fsf = layer.w1_sf_rowmajor.clone()
+    common = torch.empty_like(layer.gs_w1_gate)
+    B.moe_fold_gate_up_scales(fsf, layer.gs_w1_gate, layer.gs_w1_up, common)
+    fold = run(variant(layer.w1_fp4, fsf, common, common, layer.w2_fp4, layer.w2_sf_rowmajor, layer.gs_w2))
+    # double quantisation of the touched experts (the others do not reach the sampled tokens)
+    w1c, w1s, w2c, w2s = (t.clone() for t in (layer.w1_fp4, layer.w1_sf_rowmajor, layer.w2_fp4, layer.w2_sf_rowmajor))
+    gg, gu, g2 = (t.clone() for t in (layer.gs_w1_gate, layer.gs_w1_up, layer.gs_w2))
+    sws = torch.empty(B.moe_stage_workspace_size(), dtype=torch.uint8, device="cuda")
+    for e in touched:
+        B.moe_stage_activation(dq_w1[e][:I], w1c[e, :I], w1s[e, :I], B.MOE_SF_ROWMAJOR, gg[e:e + 1], ws=sws)
+        B.moe_stage_activation(dq_w1[e][I:], w1c[e, I:], w1s[e, I:], B.MOE_SF_ROWMAJOR, gu[e:e + 1], ws=sws)
+        B.moe_stage_activation(dq_w2[e], w2c[e], w2s[e], B.MOE_SF_ROWMAJOR, g2[e:e + 1], ws=sws)
+    double = run(variant(w1c, w1s, gg, gu, w2c, w2s, g2))
+    torch.cuda.synchronize()
+    # a checkpoint whose global scales are not the amax rule's: the BF16 weights quantised
+    # with 1.25x the layer's global scales (block scales 0.8x, no saturation); its own
+    # dequantised BF16 layer is the reference; direct = that checkpoint as is, double =
+    # dequantised and quantised again (amax rule)
+    cw1c, cw1s, cw2c, cw2s = (t.clone() for t in (layer.w1_fp4, layer.w1_sf_rowmajor, layer.w2_fp4,
+                                                 layer.w2_sf_rowmajor))
+    cgg, cgu, cg2 = (t * 1.25 for t in (layer.gs_w1_gate, layer.gs_w1_up, layer.gs_w2))
+    scratch = torch.zeros(1, dtype=torch.float32, device="cuda")
+    for e in touched:
+        w1b = workloads.expert_w1(wl, e).cuda()
+        w2b = workloads.expert_w2(wl, e).cuda()
+        B.moe_stage_activation(w1b[:I], cw1c[e, :I], cw1s[e, :I], B.MOE_SF_ROWMAJOR, scratch, gs_fixed=cgg[e:e + 1])
+        B.moe_stage_activation(w1b[I:], cw1c[e, I:], cw1s[e, I:], B.MOE_SF_ROWMAJOR, scratch, gs_fixed=cgu[e:e + 1])
+        B.moe_stage_activation(w2b, cw2c[e], cw2s[e], B.MOE_SF_ROWMAJOR, scratch, gs_fixed=cg2[e:e + 1])
+    cdq_w1 = {e: torch.cat([dq(cw1c[e, :I], cw1s[e, :I], cgg[e]), dq(cw1c[e, I:], cw1s[e, I:], cgu[e])])
+              for e in touched}
+    cdq_w2 = {e: dq(cw2c[e], cw2s[e], cg2[e]) for e in touched}
+    ref = omoe.forward_bf16(x_c.float().numpy(), ids_np, w_np, E, wl.expert_offset,
+                            lambda e: cdq_w1[e].float().cpu().numpy(), lambda e: cdq_w2[e].float().cpu().numpy(),
+                            tokens=tokens)
+    c_direct = run(variant(cw1c, cw1s, cgg, cgu, cw2c, cw2s, cg2))
+    dw1c, dw1s, dw2c, dw2s = (t.clone() for t in (cw1c, cw1s, cw2c, cw2s))
+    dgg, dgu, dg2 = (t.clone() for t in (cgg, cgu, cg2))
+    for e in touched:
+        B.moe_stage_activation(cdq_w1[e][:I], dw1c[e, :I], dw1s[e, :I], B.MOE_SF_ROWMAJOR, dgg[e:e + 1], ws=sws)
+        B.moe_stage_activation(cdq_w1[e][I:], dw1c[e, I:], dw1s[e, I:], B.MOE_SF_ROWMAJOR, dgu[e:e + 1], ws=sws)
+        B.moe_stage_activation(cdq_w2[e], dw2c[e], dw2s[e], B.MOE_SF_ROWMAJOR, dg2[e:e + 1], ws=sws)
+    c_double = run(variant(dw1c, dw1s, dgg, dgu, dw2c, dw2s, dg2))
+    torch.cuda.synchronize()
+    return {"reference": "oracle forward_bf16 on the checkpoint's NVFP4 weights dequantised to BF16",
+            "tokens": int(live.sum()), "experts": len(touched),
+            "cosine_direct_two_alphas": direct, "cosine_fold_one_alpha": fold,
+            "cosine_double_quantised": double,
+            "calibrated_checkpoint": {"global_scales": "1.25 x the amax rule",
+                                      "cosine_direct": c_direct, "cosine_double_quantised": c_double}}
 
 
 def other_configs(head, layer, fp4_peak, pk, flush, ws, R, B, steps=5, warmup=2):

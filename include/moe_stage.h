@@ -122,6 +122,21 @@ size_t moe_workspace_size(int64_t T_max, int K, int I, int E, int topk);
 moe_status moe_prepare_weights(const uint8_t* sf_rowmajor, uint8_t* sf_prepared,
                                int E, int N, int K, int kind, moe_stream_t stream);
 
+/* The pages' one-alpha handling of W1's two global scales (commits of
+ * vllm/nvfp4_cutedsl.py, "dual global scale"): per expert e, with c = max(gs_gate[e],
+ * gs_up[e]), every block scale s of the half whose global scale g is smaller becomes
+ * the UE4M3 value nearest to s * (g / c) (fp32 division, fp32 multiply, round to
+ * nearest even, saturating); gs_common[e] = c.  The L1 GEMM then takes gs_common as
+ * both its gate and up weight scales.  The layer's own path keeps two exact alphas;
+ * this is the compatibility form, for the accuracy comparison.
+ *   w1_sf:      [E, 2I, K/16] UE4M3 bytes, row-major (before moe_prepare_weights),
+ *               gate rows 0..I-1, up rows I..2I-1; folded in place (device).
+ *   gs_gate, gs_up: [E] fp32 (device); gs_common: [E] fp32 (device), written.
+ *   Experts whose two scales are equal or both zero are unchanged.  I > 0,
+ *   K % 16 == 0; MOE_ERR_INVALID_ARG for NULL pointers or non-positive sizes. */
+moe_status moe_fold_gate_up_scales(uint8_t* w1_sf, const float* gs_gate, const float* gs_up,
+                                   float* gs_common, int E, int I, int K, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Per-call path                                                              */
 /* ------------------------------------------------------------------------- */

@@ -37,7 +37,7 @@ EXPORTS = (
     "moe_stage_activation", "moe_stage_activation_to_slots", "moe_route",
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
     "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
-    "moe_set_gemm_policy", "moe_combine_rows", "moe_selftest_bounded_wait",
+    "moe_set_gemm_policy", "moe_combine_rows", "moe_selftest_bounded_wait", "moe_fold_gate_up_scales",
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
@@ -83,6 +83,7 @@ def _load():
         "moe_cast_output": (I32, [P, P, I64, I32, P]),
         "moe_combine_rows": (I32, [P, I64, P, P, I64, I32, I32, I64, P, P, P]),
         "moe_selftest_bounded_wait": (I32, [P, P, P]),
+        "moe_fold_gate_up_scales": (I32, [P, P, P, P, I32, I32, I32, P]),
         "moe_set_gemm_policy": (I32, [I32]),
         "moe_forward": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32, P, P,
                               P, P, SZ, P]),
@@ -223,6 +224,14 @@ def moe_grouped_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, I, K, w2_
 def moe_cast_output(out32, out_bf16, stream=None):
     T, K = out32.shape
     _check("moe_cast_output", _lib.moe_cast_output(_p(out32), _p(out_bf16), T, K, _stream(stream)))
+
+
+def moe_fold_gate_up_scales(w1_sf, gs_gate, gs_up, gs_common, stream=None):
+    """Fold W1's two global scales into one (see include/moe_stage.h): w1_sf [E, 2I, K/16]
+    uint8 row-major, folded in place; gs_common [E] written."""
+    E, N2, k_sf = w1_sf.shape
+    _check("moe_fold_gate_up_scales", _lib.moe_fold_gate_up_scales(
+        _p(w1_sf), _p(gs_gate), _p(gs_up), _p(gs_common), E, N2 // 2, k_sf * 16, _stream(stream)))
 
 
 def moe_selftest_bounded_wait(dev_status, dev_result, stream=None):

@@ -143,6 +143,15 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
+moe_status moe_fold_gate_up_scales(uint8_t* w1_sf, const float* gs_gate, const float* gs_up, float* gs_common,
+                                   int E, int I, int K, moe_stream_t stream) {
+  if (!w1_sf || !gs_gate || !gs_up || !gs_common || E <= 0 || I <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return launch_fold_gate_up(w1_sf, gs_gate, gs_up, gs_common, E, I, K, (cudaStream_t)stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 moe_status moe_selftest_bounded_wait(int32_t* dev_status, int32_t* dev_result, moe_stream_t stream) {
   if (!dev_status || !dev_result) return MOE_ERR_INVALID_ARG;
   return selftest_bounded_wait(dev_status, dev_result, (cudaStream_t)stream);

@@ -106,6 +106,10 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
                                  void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
                                  int64_t T, int32_t* status, cudaStream_t st, bool pdl = false);
 
+// Gate/up scale fold (set-up, quant.cu).
+cudaError_t launch_fold_gate_up(uint8_t* sf, const float* gg, const float* gu, float* common, int E, int I, int K,
+                                cudaStream_t st);
+
 // Bounded-wait self-test (selftest.cu).
 moe_status selftest_bounded_wait(int32_t* status, int32_t* result, cudaStream_t st);
 

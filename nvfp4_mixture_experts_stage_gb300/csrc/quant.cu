@@ -299,6 +299,38 @@ __global__ void __launch_bounds__(256, 4) quantize_slots_kernel(QuantArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Gate/up scale fold (set-up): the half of each expert's W1 with the smaller global
+// scale g gets its block scales multiplied by g / max(gate, up) and re-rounded to UE4M3.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) fold_gate_up_kernel(uint8_t* __restrict__ sf, const float* __restrict__ gg,
+                                                           const float* __restrict__ gu, float* __restrict__ common,
+                                                           int E, int64_t half_bytes) {
+  const int64_t n = (int64_t)E * 2 * half_bytes;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t e = i / (2 * half_bytes);
+    const bool up = ((i / half_bytes) & 1) != 0;
+    const float g_gate = __ldg(gg + e), g_up = __ldg(gu + e);
+    const float c = fmaxf(g_gate, g_up);
+    const float g = up ? g_up : g_gate;
+    if (g == c || c == 0.0f) continue;
+    const float ratio = __fdiv_rn(g, c);
+    sf[i] = (uint8_t)e4m3_byte(__fmul_rn(e4m3_value(sf[i]), ratio));
+  }
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride)
+    common[e] = fmaxf(__ldg(gg + e), __ldg(gu + e));
+}
+
+cudaError_t launch_fold_gate_up(uint8_t* sf, const float* gg, const float* gu, float* common, int E, int I, int K,
+                                cudaStream_t st) {
+  const int64_t half_bytes = (int64_t)I * (K / 16);
+  const int64_t n = (int64_t)E * 2 * half_bytes;
+  const int blocks = (int)std::min<int64_t>(std::max<int64_t>((n + 255) / 256, 1), 4096);
+  fold_gate_up_kernel<<<blocks, 256, 0, st>>>(sf, gg, gu, common, E, half_bytes);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st, bool pdl) {
   // the run kernel stores 16 code bytes at a time: it needs a 16-byte aligned code buffer
   // (the API asks for 4); 32-bit offsets need capacity * K / 2 < 2^31

@@ -226,6 +226,33 @@ def forward_bf16(x, topk_ids, topk_w, E, expert_offset, expert_w1, expert_w2, to
     return out
 
 
+def fold_gate_up_scales(w1_sf, gs_gate, gs_up):
+    """The pages' gate/up handling (commits of vllm/nvfp4_cutedsl.py, "dual global scale"):
+    both halves of W1 are normalised to the larger of the two global scales, and the
+    ratio of the smaller one to it is folded into that half's block scales -- one fp32
+    multiply of each decoded scale by the ratio, rounded back to UE4M3 (nearest, ties to
+    even, saturating).  The L1 GEMM then needs one alpha per expert (gs_x * common).
+
+    w1_sf: [E, 2I, K/16] row-major UE4M3 bytes, gate rows then up rows; gs_gate, gs_up:
+    [E] fp32.  Returns (folded scales, common global scale [E] = max(gs_gate, gs_up));
+    an expert whose two scales are equal (or both zero) is unchanged."""
+    w1_sf = np.asarray(w1_sf, np.uint8)
+    E, N2, _ = w1_sf.shape
+    I = N2 // 2
+    gg = np.asarray(gs_gate, F32)
+    gu = np.asarray(gs_up, F32)
+    common = np.maximum(gg, gu).astype(F32)
+    out = w1_sf.copy()
+    for e in range(E):
+        for rows, g in ((slice(0, I), gg[e]), (slice(I, N2), gu[e])):
+            if g == common[e] or common[e] == 0:
+                continue
+            ratio = F32(g) / F32(common[e])                       # fp32, round to nearest even
+            scaled = nvfp4.e4m3_decode(out[e, rows]).astype(F32) * ratio   # fp32 multiply
+            out[e, rows] = nvfp4.e4m3_encode_satfinite(scaled)
+    return out, common
+
+
 def quantize_weights(w1, w2):
     """Quantise BF16 expert weights the way the layer consumes them.
 

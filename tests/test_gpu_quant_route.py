@@ -259,3 +259,24 @@ def test_prepare_weights_layout():
         inter = np.concatenate([np.concatenate([sf1[e, 64 * j:64 * j + 64], sf1[e, I + 64 * j:I + 64 * j + 64]])
                                 for j in range(I // 64)])
         assert np.array_equal(q.unswizzle(g1[e], 2 * I, K // 16), inter)
+
+
+@pytest.mark.parametrize("gg,gu", [(1e-2, 6e-3), (2e-3, 8e-3), (5e-4, 5e-4), (0.0, 0.0), (1e-2, 1e-9),
+                                   (3e-3, 3e-3 / 1024), (7.0, 0.0)])
+def test_fold_gate_up_scales_bit_exact(gg, gu):
+    """The pages' one-alpha W1 form: the GPU fold of every scale byte equals the oracle's."""
+    from oracle import moe as omoe
+    E, I, K = 3, 128, 2048
+    r = np.random.default_rng(int(gg * 1e4) + int(gu * 1e6) + 11)
+    sf = r.integers(0, 0x7F, (E, 2 * I, K // 16)).astype(np.uint8)
+    sf[:, 0, :127] = np.arange(127)          # every finite byte in both halves
+    sf[:, I, :127] = np.arange(127)
+    g_gate = np.array([gg, gg * 0.5, 1e-3], np.float32)
+    g_up = np.array([gu, gu, 1e-3], np.float32)
+    d = torch.from_numpy(sf.copy()).cuda()
+    common = torch.zeros(E, dtype=torch.float32, device="cuda")
+    B.moe_fold_gate_up_scales(d, torch.from_numpy(g_gate).cuda(), torch.from_numpy(g_up).cuda(), common)
+    torch.cuda.synchronize()
+    ref, rcommon = omoe.fold_gate_up_scales(sf, g_gate, g_up)
+    assert np.array_equal(d.cpu().numpy(), ref)
+    assert np.array_equal(common.cpu().numpy(), rcommon)

@@ -242,3 +242,78 @@ def test_bf16_reference_layer_brute_force_and_close_to_nvfp4():
     out = omoe.forward(x, ids, w, wl.E, wl.expert_offset, W)["out"]
     cos = float((out * ref).sum() / np.sqrt((out * out).sum() * (ref * ref).sum()))
     assert cos > 0.95   # 0.975 here: the tiny inputs carry 1 % outliers at 20x
+
+
+# ------------------------------------------------------------- gate/up scale fold
+def _nearest_e4m3_brute(v):
+    """Nearest UE4M3 byte to v >= 0 by search over every finite byte (torch's float8
+    view decodes them), ties to the even byte (even mantissa)."""
+    best, best_d = None, None
+    for b in range(0x7F):
+        d = abs(_scale(b) - Fraction(float(v)))
+        if best is None or d < best_d or (d == best_d and b % 2 == 0):
+            best, best_d = b, d
+    return best
+
+
+def test_fold_equal_scales_is_identity():
+    r = np.random.default_rng(40)
+    sf = r.integers(0, 0x7F, (3, 16, 4)).astype(np.uint8)
+    g = np.array([1e-3, 2.5e-4, 0.0], F32)
+    out, common = moe.fold_gate_up_scales(sf, g, g)
+    assert np.array_equal(out, sf) and np.array_equal(common, g)
+
+
+def test_fold_power_of_two_ratio_shifts_the_exponent():
+    """gs_up = gs_gate / 4: every up scale whose exponent field is at least 3 drops by two
+    binades (byte - 16) and the gate half is untouched; the common scale is gs_gate."""
+    sf = np.tile(np.arange(0, 0x7F, dtype=np.uint8), (2, 1)).reshape(1, 2, 127)   # gate row, up row
+    out, common = moe.fold_gate_up_scales(sf, np.array([8e-3], F32), np.array([2e-3], F32))
+    assert common[0] == F32(8e-3)
+    assert np.array_equal(out[0, 0], sf[0, 0])
+    normal = np.arange(127) >= 3 * 8
+    assert np.array_equal(out[0, 1][normal], (np.arange(127)[normal] - 16).astype(np.uint8))
+
+
+@pytest.mark.parametrize("ratio_num,ratio_den", [(3, 5), (1, 3), (7, 1000), (1, 1 << 20)])
+def test_fold_matches_nearest_search_on_every_byte(ratio_num, ratio_den):
+    """Every finite scale byte times an arbitrary ratio lands on the nearest UE4M3 value
+    (brute-force search over all bytes, ties even), the gate half being the larger."""
+    gate = F32(1e-2)
+    up = F32(F32(gate) * F32(ratio_num / ratio_den))
+    sf = np.tile(np.arange(0, 0x7F, dtype=np.uint8), (2, 1)).reshape(1, 2, 127)
+    out, common = moe.fold_gate_up_scales(sf, np.array([gate]), np.array([up]))
+    ratio = F32(up) / F32(gate)
+    for b in range(0x7F):
+        v = F32(F32(float(_scale(b))) * ratio)
+        assert out[0, 1, b] == _nearest_e4m3_brute(v), (b, float(v))
+    assert np.array_equal(out[0, 0], sf[0, 0])
+    # the folded weights, at the common scale, equal the original ones within the
+    # UE4M3 rounding of the folded scale (half a step: 2**-4 relative for normal values)
+    orig = np.array([float(_scale(b)) for b in range(127)]) * float(up)
+    new = np.array([float(_scale(b)) for b in out[0, 1]]) * float(common[0])
+    normal = new >= 2.0 ** -6 * float(common[0])
+    assert np.all(np.abs(new - orig)[normal] <= 2.0 ** -4 * orig[normal] * (1 + 1e-6))
+
+
+def test_fold_gives_one_alpha_l1_close_to_two_alphas():
+    """L1 with the folded scales and one alpha per expert stays within the UE4M3 rounding
+    of the exact two-alpha L1 (the pages' accuracy trade-off)."""
+    wl = workloads.WORKLOADS["tiny"]
+    W = _tiny_weights(wl)
+    x = workloads.activations(wl).float().numpy()
+    ids, w = workloads.routing(wl)
+    rt = route(ids, w, wl.E, wl.expert_offset)
+    a_codes, a_sf, gs_x = q.quantize(q.bf16_round(x))
+    ac = np.zeros((len(rt["slot_token"]), wl.K // 2), np.uint8)
+    asf = np.zeros((len(rt["slot_token"]), wl.K // 16), np.uint8)
+    valid = rt["slot_token"] >= 0
+    ac[valid], asf[valid] = a_codes[rt["slot_token"][valid]], a_sf[rt["slot_token"][valid]]
+    g2, u2 = moe.gemm_l1(ac, asf, gs_x, rt, W["w1_codes"], W["w1_sf"], W["gs_w1_gate"], W["gs_w1_up"])
+    fsf, common = moe.fold_gate_up_scales(W["w1_sf"], W["gs_w1_gate"], W["gs_w1_up"])
+    assert not np.array_equal(fsf, W["w1_sf"])      # the two halves' scales differ here
+    g1, u1 = moe.gemm_l1(ac, asf, gs_x, rt, W["w1_codes"], fsf, common, common)
+    for a, b in ((g1, g2), (u1, u2)):
+        a, b = a[valid].astype(np.float64), b[valid].astype(np.float64)
+        assert np.abs(a - b).max() <= 0.1 * np.abs(b).max()
+        assert float((a * b).sum() / np.sqrt((a * a).sum() * (b * b).sum())) > 0.99
