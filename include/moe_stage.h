@@ -122,6 +122,24 @@ size_t moe_workspace_size(int64_t T_max, int K, int I, int E, int topk);
 moe_status moe_prepare_weights(const uint8_t* sf_rowmajor, uint8_t* sf_prepared,
                                int E, int N, int K, int kind, moe_stream_t stream);
 
+/* Quantise a rank's BF16 expert weights to the form the layer consumes, on the device
+ * (the pages' finalize_weights / weight_transform step, for BF16 inputs): per expert,
+ * the gate rows, the up rows and the down projection each get their own global scale
+ * (amax / 2688) and are block-quantised as moe_stage_activation does; the scales are
+ * then rearranged as moe_prepare_weights does.
+ *   w1: [E, 2I, K] BF16 (gate rows 0..I-1, up rows I..2I-1), w2: [E, K, I] BF16,
+ *       16-byte aligned (device).
+ *   w1_fp4 [E, 2I, K/2], w2_fp4 [E, K, I/2]: codes; w1_sf, w2_sf: E*2I*K/16 and
+ *       E*K*I/16 bytes in the GEMMs' layouts; gs_w1_gate, gs_w1_up, gs_w2: [E] fp32.
+ *   ws: moe_quantize_weights_workspace_size(E, I, K) bytes of scratch (the row-major
+ *       scales pass through it).
+ *   I % 64 == 0, K % 128 == 0.  Stream-ordered, no host sync; set-up, not timed. */
+size_t moe_quantize_weights_workspace_size(int E, int I, int K);
+moe_status moe_quantize_weights(const void* w1, const void* w2, int E, int I, int K,
+                                uint8_t* w1_fp4, uint8_t* w1_sf, float* gs_w1_gate, float* gs_w1_up,
+                                uint8_t* w2_fp4, uint8_t* w2_sf, float* gs_w2,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* The pages' one-alpha handling of W1's two global scales (commits of
  * vllm/nvfp4_cutedsl.py, "dual global scale"): per expert e, with c = max(gs_gate[e],
  * gs_up[e]), every block scale s of the half whose global scale g is smaller becomes

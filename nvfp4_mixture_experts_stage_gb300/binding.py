@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
     "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
     "moe_set_gemm_policy", "moe_combine_rows", "moe_selftest_bounded_wait", "moe_fold_gate_up_scales",
+    "moe_quantize_weights_workspace_size", "moe_quantize_weights",
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
@@ -84,6 +85,8 @@ def _load():
         "moe_combine_rows": (I32, [P, I64, P, P, I64, I32, I32, I64, P, P, P]),
         "moe_selftest_bounded_wait": (I32, [P, P, P]),
         "moe_fold_gate_up_scales": (I32, [P, P, P, P, I32, I32, I32, P]),
+        "moe_quantize_weights_workspace_size": (ctypes.c_size_t, [I32, I32, I32]),
+        "moe_quantize_weights": (I32, [P, P, I32, I32, I32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
         "moe_set_gemm_policy": (I32, [I32]),
         "moe_forward": (I32, [P, I64, I32, I32, I32, P, P, I32, I32, ctypes.POINTER(MoeWeights), P, I32, P, P,
                               P, P, SZ, P]),
@@ -224,6 +227,19 @@ def moe_grouped_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, I, K, w2_
 def moe_cast_output(out32, out_bf16, stream=None):
     T, K = out32.shape
     _check("moe_cast_output", _lib.moe_cast_output(_p(out32), _p(out_bf16), T, K, _stream(stream)))
+
+
+def moe_quantize_weights_workspace_size(E, I, K):
+    return int(_lib.moe_quantize_weights_workspace_size(E, I, K))
+
+
+def moe_quantize_weights(w1, w2, w1_fp4, w1_sf, gs_w1_gate, gs_w1_up, w2_fp4, w2_sf, gs_w2, ws, stream=None):
+    """BF16 expert weights w1 [E, 2I, K], w2 [E, K, I] -> NVFP4 codes, prepared scales and
+    global scales (see include/moe_stage.h)."""
+    E, N2, K = w1.shape
+    _check("moe_quantize_weights", _lib.moe_quantize_weights(
+        _p(w1), _p(w2), E, N2 // 2, K, _p(w1_fp4), _p(w1_sf), _p(gs_w1_gate), _p(gs_w1_up), _p(w2_fp4),
+        _p(w2_sf), _p(gs_w2), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_fold_gate_up_scales(w1_sf, gs_gate, gs_up, gs_common, stream=None):

@@ -143,6 +143,47 @@ const char* moe_status_string(moe_status s) {
   return "unknown status";
 }
 
+size_t moe_quantize_weights_workspace_size(int E, int I, int K) {
+  if (E < 1 || I < 1 || K < 1) return 0;
+  return align256(moe_stage_workspace_size()) + align256((size_t)E * 2 * I * (K / 16)) +
+         align256((size_t)E * K * (I / 16));
+}
+
+moe_status moe_quantize_weights(const void* w1, const void* w2, int E, int I, int K, uint8_t* w1_fp4, uint8_t* w1_sf,
+                                float* gs_w1_gate, float* gs_w1_up, uint8_t* w2_fp4, uint8_t* w2_sf, float* gs_w2,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!w1 || !w2 || !w1_fp4 || !w1_sf || !gs_w1_gate || !gs_w1_up || !w2_fp4 || !w2_sf || !gs_w2 || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (E < 1 || I < 1 || K < 1 || !aligned(w1, 16) || !aligned(w2, 16)) return MOE_ERR_INVALID_ARG;
+  if (I % 64 || K % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < moe_quantize_weights_workspace_size(E, I, K)) return MOE_ERR_WORKSPACE;
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  void* sws = p;
+  p += align256(moe_stage_workspace_size());
+  uint8_t* sf1 = p;  // row-major [E, 2I, K/16]
+  p += align256((size_t)E * 2 * I * (K / 16));
+  uint8_t* sf2 = p;  // row-major [E, K, I/16]
+  const uint8_t* x1 = static_cast<const uint8_t*>(w1);
+  const uint8_t* x2 = static_cast<const uint8_t*>(w2);
+  const size_t sws_bytes = moe_stage_workspace_size();
+  for (int e = 0; e < E; ++e) {
+    for (int h = 0; h < 2; ++h) {  // gate rows, then up rows
+      const int64_t r0 = (int64_t)e * 2 * I + (int64_t)h * I;
+      moe_status s = moe_stage_activation(x1 + r0 * K * 2, I, K, K, w1_fp4 + r0 * (K / 2), sf1 + r0 * (K / 16),
+                                          MOE_SF_ROWMAJOR, (h ? gs_w1_up : gs_w1_gate) + e, nullptr, sws, sws_bytes,
+                                          nullptr, stream);
+      if (s != MOE_OK) return s;
+    }
+    const int64_t r2 = (int64_t)e * K;
+    moe_status s = moe_stage_activation(x2 + r2 * I * 2, K, I, I, w2_fp4 + r2 * (I / 2), sf2 + r2 * (I / 16),
+                                        MOE_SF_ROWMAJOR, gs_w2 + e, nullptr, sws, sws_bytes, nullptr, stream);
+    if (s != MOE_OK) return s;
+  }
+  moe_status s = moe_prepare_weights(sf1, w1_sf, E, 2 * I, K, MOE_PREP_W1, stream);
+  if (s != MOE_OK) return s;
+  return moe_prepare_weights(sf2, w2_sf, E, K, I, MOE_PREP_W2, stream);
+}
+
 moe_status moe_fold_gate_up_scales(uint8_t* w1_sf, const float* gs_gate, const float* gs_up, float* gs_common,
                                    int E, int I, int K, moe_stream_t stream) {
   if (!w1_sf || !gs_gate || !gs_up || !gs_common || E <= 0 || I <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;

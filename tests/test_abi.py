@@ -87,6 +87,10 @@ def test_argument_checks_fail_before_any_device_work(B):
                                    null, null, null, null, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_cast_output(null, null, 4, 7, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_selftest_bounded_wait(null, null, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_weights(null, null, 2, 128, 256, null, null, null, null, null, null, null, null, 0,
+                                    null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_fold_gate_up_scales(null, null, null, null, 2, 128, 256, null) == B.MOE_ERR_INVALID_ARG
+    assert B.moe_quantize_weights_workspace_size(2, 128, 256) >= 2 * 256 * 16 + 2 * 256 * 8
     assert lib.moe_combine_rows(null, 8, null, null, 4, 2, 7, 16, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_combine_rows(null, 8, null, null, 4, 2, 8, 16, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_combine_rows(null, 8, null, null, 0, 2, 8, 16, null, null, null) == B.MOE_OK  # nothing to do

@@ -280,3 +280,34 @@ def test_fold_gate_up_scales_bit_exact(gg, gu):
     ref, rcommon = omoe.fold_gate_up_scales(sf, g_gate, g_up)
     assert np.array_equal(d.cpu().numpy(), ref)
     assert np.array_equal(common.cpu().numpy(), rcommon)
+
+
+
+def test_quantize_weights_on_device_bit_exact():
+    """moe_quantize_weights: codes and global scales equal the oracle's per-projection
+    quantisation; the scales equal moe_prepare_weights of the oracle's row-major ones."""
+    from oracle import moe as omoe
+    E, I, K = 3, 128, 256
+    r = np.random.default_rng(12)
+    w1 = q.bf16_round((r.standard_normal((E, 2 * I, K)) * 0.02).astype(np.float32))
+    w2 = q.bf16_round((r.standard_normal((E, K, I)) * 0.02).astype(np.float32))
+    w1[1, :I] = q.bf16_round(w1[1, :I] * 50)  # gate and up of expert 1 on different scales
+    ref = omoe.quantize_weights(w1, w2)
+    t = lambda a: torch.from_numpy(a).to(torch.bfloat16).cuda()
+    u8 = lambda *sh: torch.zeros(*sh, dtype=torch.uint8, device="cuda")
+    f32 = lambda n: torch.zeros(n, dtype=torch.float32, device="cuda")
+    w1c, w1s, w2c, w2s = u8(E, 2 * I, K // 2), u8(E * 2 * I * K // 16), u8(E, K, I // 2), u8(E * K * I // 16)
+    gg, gu, g2 = f32(E), f32(E), f32(E)
+    ws = u8(B.moe_quantize_weights_workspace_size(E, I, K))
+    B.moe_quantize_weights(t(w1), t(w2), w1c, w1s, gg, gu, w2c, w2s, g2, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(w1c.cpu().numpy(), ref["w1_codes"])
+    assert np.array_equal(w2c.cpu().numpy(), ref["w2_codes"])
+    for got, key in ((gg, "gs_w1_gate"), (gu, "gs_w1_up"), (g2, "gs_w2")):
+        assert np.array_equal(got.cpu().numpy(), ref[key])
+    e1 = torch.empty_like(w1s)
+    e2 = torch.empty_like(w2s)
+    B.moe_prepare_weights(torch.from_numpy(ref["w1_sf"]).cuda(), e1, E, 2 * I, K, B.MOE_PREP_W1)
+    B.moe_prepare_weights(torch.from_numpy(ref["w2_sf"]).cuda(), e2, E, K, I, B.MOE_PREP_W2)
+    torch.cuda.synchronize()
+    assert torch.equal(w1s, e1) and torch.equal(w2s, e2)
