@@ -76,6 +76,31 @@ def test_forward_matches_oracle(wl, mode):
     assert np.all(got[none_local] == 0)
 
 
+def test_forward_maximum_experts_and_topk():
+    """The API's limits: 256 local experts (most with a handful of slots, some empty) and
+    top-32 routing."""
+    wl = workloads.small("maxes", T=40, K=256, I=64, E=256, topk=32)
+    W = oracle_weights(wl)
+    gs_h = workloads.fixed_gs_h(wl)
+    got, _, x, ids, w = _run(wl, W, B.MOE_GS_FIXED, gs_h)
+    ref = omoe.forward(x.float().numpy(), ids, w, wl.E, wl.expert_offset, W, gs_h=gs_h)
+    assert_layer_close(got, ref["out"], wl.name)
+
+
+def test_forward_empty_batch():
+    """T = 0: nothing to do, status OK, no launch touches the (empty) buffers."""
+    wl = workloads.small("empty_src", T=8, K=256, I=64, E=4, topk=2)
+    W = oracle_weights(wl)
+    layer = _layer(W, wl)
+    fw = R.Forward(layer, 0, B.MOE_GS_DYNAMIC)
+    x = torch.zeros(0, wl.K, dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros(0, wl.topk, dtype=torch.int32, device="cuda")
+    w = torch.zeros(0, wl.topk, dtype=torch.float32, device="cuda")
+    out = fw(x, ids, w)
+    torch.cuda.synchronize()
+    assert out.shape == (0, wl.K) and fw.status.item() == 0
+
+
 def test_forward_graph_capture_and_replay():
     wl = SMALL[1]
     W = oracle_weights(wl)
