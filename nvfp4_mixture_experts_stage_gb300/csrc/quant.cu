@@ -425,20 +425,42 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
     float acc[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
-    for (int j = 0; j < topk; ++j) {
-      const int32_t s = __ldg(pair_slot + t * topk + j);
-      if (s < 0) continue;
-      if (s >= capacity) {
-        set_status(status, MOE_ERR_DEVICE_INDEX);
-        continue;
-      }
-      const float wj = __ldg(w + t * topk + j);
-      const uint4 q = __ldg(y + (int64_t)s * ld_vec + v);
+    auto add = [&](float wj, const uint4& q) {
       const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         acc[2 * c] = __fadd_rn(acc[2 * c], __fmul_rn(wj, bf16lo(qw[c])));
         acc[2 * c + 1] = __fadd_rn(acc[2 * c + 1], __fmul_rn(wj, bf16hi(qw[c])));
+      }
+    };
+    if (topk <= 8) {
+      // the token's slots, then all its rows' loads in flight together; summed in pair order
+      int32_t sj[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sj[j] = j < topk ? __ldg(pair_slot + t * topk + j) : -1;
+      float wj[8];
+      uint4 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (sj[j] >= capacity) {
+          set_status(status, MOE_ERR_DEVICE_INDEX);
+          sj[j] = -1;
+        }
+        wj[j] = sj[j] >= 0 ? __ldg(w + t * topk + j) : 0.0f;
+        q[j] = sj[j] >= 0 ? __ldg(y + (int64_t)sj[j] * ld_vec + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (sj[j] >= 0) add(wj[j], q[j]);
+    } else {
+      for (int j = 0; j < topk; ++j) {
+        const int32_t s = __ldg(pair_slot + t * topk + j);
+        if (s < 0) continue;
+        if (s >= capacity) {
+          set_status(status, MOE_ERR_DEVICE_INDEX);
+          continue;
+        }
+        add(__ldg(w + t * topk + j), __ldg(y + (int64_t)s * ld_vec + v));
       }
     }
     out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),

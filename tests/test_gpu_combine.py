@@ -42,7 +42,8 @@ def _case(T, K, E, topk, offset, n_global, seed, y_scale=1.0):
 
 
 @pytest.mark.parametrize("T,K,E,topk,offset,n_global", [(37, 256, 8, 2, 0, 8), (64, 4096, 48, 8, 144, 384),
-                                                         (300, 7168, 48, 8, 0, 48), (5, 8, 4, 3, 4, 12)])
+                                                         (300, 7168, 48, 8, 0, 48), (5, 8, 4, 3, 4, 12),
+                                                         (20, 256, 32, 12, 0, 32)])
 def test_combine_bit_exact(T, K, E, topk, offset, n_global):
     got, ref, rt = _case(T, K, E, topk, offset, n_global, seed=T + K)
     assert np.array_equal(got, ref)
