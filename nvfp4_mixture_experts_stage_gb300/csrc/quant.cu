@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     uint4 v[U];
     int64_t row[U];
     int col[U];
+    bool live[U];  // the segment belongs to a row that is quantised (warp-uniform)
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t s = base + u * nwarps;
@@ -120,8 +121,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
       cur_row += drow;
       cur_seg += dseg;
       if (cur_seg >= nseg) { cur_seg -= nseg; ++cur_row; }
-      bool ok = s < total && col[u] < a.K;
-      if (ok && DST == kDstMasked) ok = __ldg(a.slot_token + row[u]) >= 0;
+      live[u] = s < total;
+      if (live[u] && DST == kDstMasked) live[u] = __ldg(a.slot_token + row[u]) >= 0;
+      const bool ok = live[u] && col[u] < a.K;
       v[u] = ok ? __ldcs(a.x + row[u] * a.ld_vec + (col[u] >> 3)) : make_uint4(0, 0, 0, 0);
       if (!ok) col[u] = -1;
     }
@@ -136,6 +138,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      if (!live[u]) continue;  // a padding row (masked) or past the end: the whole warp skips it
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       float f[8];
 #pragma unroll

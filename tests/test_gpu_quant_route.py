@@ -311,3 +311,34 @@ def test_quantize_weights_on_device_bit_exact():
     B.moe_prepare_weights(torch.from_numpy(ref["w2_sf"]).cuda(), e2, E, K, I, B.MOE_PREP_W2)
     torch.cuda.synchronize()
     assert torch.equal(w1s, e1) and torch.equal(w2s, e2)
+
+
+@pytest.mark.parametrize("cap,I,big", [(384, 192, False), (256, 3072, True), (128, 64, False)])
+def test_requant_bit_exact_on_masked_rows(cap, I, big):
+    """moe_requant (the dynamic h scale's pass, teacher-forced): given BF16 h and the max
+    |h| over the valid rows, the codes, swizzled scales and the h global scale equal the
+    oracle's quantisation of the valid rows; padding rows are not written."""
+    r = np.random.default_rng(cap + I)
+    h = q.bf16_round(r.standard_normal((cap, I)).astype(np.float32))
+    if big:
+        h[5] = q.bf16_round(h[5] * 1e4)
+    st = np.where(r.random(cap) < 0.6, np.arange(cap), -1).astype(np.int32)
+    st[5] = 5
+    valid = st >= 0
+    amax = np.float32(np.abs(h[valid]).max())
+    hd = torch.from_numpy(h).to(torch.bfloat16).cuda()
+    codes = torch.zeros(cap, I // 2, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(cap * I // 16, dtype=torch.uint8, device="cuda")
+    gs = torch.zeros(1, dtype=torch.float32, device="cuda")
+    stat = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_requant(hd, torch.from_numpy(st).cuda(), torch.tensor([amax], device="cuda"), gs, codes, sf, dev_status=stat)
+    torch.cuda.synchronize()
+    assert stat.item() == 0
+    rc, rs, rg = q.quantize(h[valid])
+    assert np.float32(gs.item()) == rg
+    got = codes.cpu().numpy()
+    assert np.array_equal(got[valid], rc)
+    assert not got[~valid].any()
+    got_sf = q.unswizzle(sf.cpu().numpy(), cap, I // 16)
+    assert np.array_equal(got_sf[valid], rs)
+    assert not got_sf[~valid].any()
