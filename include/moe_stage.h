@@ -294,7 +294,8 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const 
  *   MOE_GEMM_AUTO      (default) the weight-streaming kernel when the slot capacity
  *                      implies at most 64 slots per local expert on average
  *                      (capacity - 127*E <= 64*E) and the contraction is <= 4096,
- *                      the tiled kernel otherwise;
+ *                      the tiled kernels otherwise (as MOE_GEMM_TILED: L1 on single
+ *                      SMs, L2's 256-wide tiles on SM pairs);
  *   MOE_GEMM_TILED     always a tiled kernel, slots on the MMA's M side: L1 in tiles
  *                      of 128 slot rows x 256 weight rows on single SMs; L2 in tiles
  *                      of 256 slot rows x 256 weight rows on pairs of SMs (a cluster
