@@ -37,18 +37,33 @@ import workloads  # noqa: E402
 METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 peak"
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture
-# (profiles/gemm_l1_stream_decode.md), valid only for the GEMM sources it was taken on.
-NCU_TRAFFIC = {"gemm_l1": {"bytes": 673994496, "sources_sha256_16": "c90dac2ab5142603"}}
+# (profiles/gemm_l1_stream_decode.md), keyed by (workload, GEMM policy, stage) and valid
+# only while the files that kernel is compiled from hash to the captured ones.
+NCU_TRAFFIC = {
+    ("decode", "auto", "gemm_l1"): {
+        "bytes": 673994496,
+        "kernel_sources": ("gemm_stream.cu", "tcgen05.cuh", "common.cuh"),
+        "sources_sha256_16": "e2703825511dc62a",
+    },
+}
 
 
-def gemm_sources_hash():
+def kernel_sources_hash(files):
     import hashlib
     h = hashlib.sha256()
-    # the files holding the grouped-GEMM kernels' code (kernels.cuh only declares launchers)
-    for f in ("gemm.cu", "gemm_pair.cu", "gemm_tiled.cuh", "gemm_stream.cu", "tcgen05.cuh", "common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "nvfp4_mixture_experts_stage_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, policy, stage):
+    tr = NCU_TRAFFIC.get((workload, policy, stage))
+    if tr is None or kernel_sources_hash(tr["kernel_sources"]) != tr["sources_sha256_16"]:
+        return None
+    return tr["bytes"]
+
+
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -424,8 +439,7 @@ def run_ours(args, ws, rank, local):
     dom_ms = stage_ms[dom]
     dom_bytes = alg["l1_bytes"] if dom == "gemm_l1" else alg["l2_bytes"]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get(dom)
-    traffic = tr["bytes"] if tr and tr["sources_sha256_16"] == gemm_sources_hash() else None
+    traffic = ncu_traffic(args.workload, args.gemm_policy, dom)
     gemm_ms = stage_ms["gemm_l1"] + stage_ms["gemm_l2"]
     gemm_tflops = (alg["flops_l1"] + alg["flops_l2"]) / (gemm_ms * 1e-3) / 1e12
 

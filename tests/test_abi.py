@@ -97,3 +97,20 @@ def test_argument_checks_fail_before_any_device_work(B):
     w = B.MoeWeights()
     assert lib.moe_forward(null, 4, 256, 100, 8, null, null, 2, 0, ctypes.byref(w), null, 0, null, null, null,
                            null, 0, null) in (B.MOE_ERR_INVALID_ARG, B.MOE_ERR_UNSUPPORTED_SHAPE)
+
+
+def test_bench_traffic_is_keyed_by_workload_policy_and_kernel_sources():
+    """The ncu DRAM figure belongs to one kernel on one workload: other workloads,
+    policies or stages get none, and an edit to the kernel's sources drops it."""
+    import bench
+    (wl, pol, stage), tr = next(iter(bench.NCU_TRAFFIC.items()))
+    assert bench.ncu_traffic("prefill", pol, stage) is None
+    assert bench.ncu_traffic(wl, "tiled", stage) is None
+    assert bench.ncu_traffic(wl, pol, "gemm_l2") is None
+    saved = dict(tr)
+    try:
+        tr["sources_sha256_16"] = "0" * 16
+        assert bench.ncu_traffic(wl, pol, stage) is None
+    finally:
+        tr.clear()
+        tr.update(saved)
