@@ -401,6 +401,22 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E,
  * the launch fails; takes about one second of device time. */
 moe_status moe_selftest_bounded_wait(int32_t* dev_status, int32_t* dev_result, moe_stream_t stream);
 
+/* Self-test of the two code encoders (no counterpart on the commit pages; the encodings
+ * are those of the pages' "NVFP4 quantisation" commits: E2M1 codes round to the nearest
+ * of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with the sign in bit 3, UE4M3 block scales round to
+ * nearest and saturate at 448).  For i < n the fp32 value v with bit pattern
+ * first_pattern + i is encoded exactly as the quantisers, the requantiser and the L1
+ * requant epilogue encode a scaled value and a block scale:
+ *   e2m1_codes[i] = E2M1 code of v (round to nearest, ties to the even magnitude index,
+ *                   saturating at 6; bit 3 = sign bit of v, also when v rounds to zero);
+ *   e4m3_bytes[i] = UE4M3 byte of v (round to nearest even, saturating at 448 = 0x7E;
+ *                   defined for v >= 0, the only values the library encodes).
+ * NaN patterns give unspecified bytes.  Both outputs are device buffers of n bytes owned
+ * by the caller.  Returns MOE_ERR_INVALID_ARG for n < 0, NULL outputs with n > 0, or a
+ * range past pattern 0xFFFFFFFF; MOE_ERR_CUDA if the launch fails. */
+moe_status moe_selftest_codecs(uint32_t first_pattern, int64_t n, uint8_t* e2m1_codes, uint8_t* e4m3_bytes,
+                               moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,7 +38,7 @@ EXPORTS = (
     "moe_grouped_gemm_l1", "moe_requant", "moe_grouped_gemm_l2",
     "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
     "moe_set_gemm_policy", "moe_combine_rows", "moe_selftest_bounded_wait", "moe_fold_gate_up_scales",
-    "moe_quantize_weights_workspace_size", "moe_quantize_weights",
+    "moe_quantize_weights_workspace_size", "moe_quantize_weights", "moe_selftest_codecs",
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
@@ -84,6 +84,7 @@ def _load():
         "moe_cast_output": (I32, [P, P, I64, I32, P]),
         "moe_combine_rows": (I32, [P, I64, P, P, I64, I32, I32, I64, P, P, P]),
         "moe_selftest_bounded_wait": (I32, [P, P, P]),
+        "moe_selftest_codecs": (I32, [ctypes.c_uint32, I64, P, P, P]),
         "moe_fold_gate_up_scales": (I32, [P, P, P, P, I32, I32, I32, P]),
         "moe_quantize_weights_workspace_size": (ctypes.c_size_t, [I32, I32, I32]),
         "moe_quantize_weights": (I32, [P, P, I32, I32, I32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
@@ -255,6 +256,16 @@ def moe_selftest_bounded_wait(dev_status, dev_result, stream=None):
     time; afterwards dev_status holds MOE_ERR_TIMEOUT and dev_result (2 int32) [1, 1]."""
     _check("moe_selftest_bounded_wait", _lib.moe_selftest_bounded_wait(_p(dev_status), _p(dev_result),
                                                                        _stream(stream)))
+
+
+def moe_selftest_codecs(first_pattern, e2m1_codes, e4m3_bytes, stream=None):
+    """Encoder self-test (see include/moe_stage.h): for the fp32 bit patterns
+    first_pattern .. first_pattern + n - 1 (n = e2m1_codes.numel()), the device's E2M1
+    code and UE4M3 byte of each value, written to the two uint8 device tensors."""
+    n = e2m1_codes.numel()
+    assert e4m3_bytes.numel() == n
+    _check("moe_selftest_codecs", _lib.moe_selftest_codecs(first_pattern, n, _p(e2m1_codes), _p(e4m3_bytes),
+                                                           _stream(stream)))
 
 
 def moe_combine_rows(y_rows, pair_slot, topk_w, out_bf16, capacity=None, dev_status=None, stream=None):

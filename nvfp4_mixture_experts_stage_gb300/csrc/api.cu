@@ -198,6 +198,13 @@ moe_status moe_selftest_bounded_wait(int32_t* dev_status, int32_t* dev_result, m
   return selftest_bounded_wait(dev_status, dev_result, (cudaStream_t)stream);
 }
 
+moe_status moe_selftest_codecs(uint32_t first_pattern, int64_t n, uint8_t* e2m1_codes, uint8_t* e4m3_bytes,
+                               moe_stream_t stream) {
+  if (n < 0 || (n > 0 && (!e2m1_codes || !e4m3_bytes))) return MOE_ERR_INVALID_ARG;
+  if ((uint64_t)first_pattern + (uint64_t)n > (1ull << 32)) return MOE_ERR_INVALID_ARG;
+  return selftest_codecs(first_pattern, n, e2m1_codes, e4m3_bytes, (cudaStream_t)stream);
+}
+
 int moe_set_gemm_policy(int policy) {
   if (policy < MOE_GEMM_AUTO || policy > MOE_GEMM_TILED_PAIR) return -1;
   return set_gemm_policy(policy);

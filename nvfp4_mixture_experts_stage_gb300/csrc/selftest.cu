@@ -1,7 +1,11 @@
-// Self-test of the bounded waits every pipeline role of the GEMM kernels uses: a wait
-// on an mbarrier that nothing completes must give up after the limit, report
-// MOE_ERR_TIMEOUT and raise the block's abort flag, and another role's wait must then
-// return through that flag.
+// Self-tests of device pieces that no layer call exposes on its own:
+//   * the bounded waits every pipeline role of the GEMM kernels uses: a wait on an
+//     mbarrier that nothing completes must give up after the limit, report
+//     MOE_ERR_TIMEOUT and raise the block's abort flag, and another role's wait must
+//     then return through that flag;
+//   * the two code encoders of the quantisers and the requant epilogue (E2M1 of a
+//     scaled value, UE4M3 of a block scale), evaluated on arbitrary fp32 bit patterns
+//     so that a test can sweep every input.
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -33,6 +37,23 @@ __global__ void __launch_bounds__(64, 1) selftest_bounded_wait_kernel(int32_t* s
 
 moe_status selftest_bounded_wait(int32_t* status, int32_t* result, cudaStream_t st) {
   selftest_bounded_wait_kernel<<<1, 64, 0, st>>>(status, result);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Pattern first + i for i < n: E2M1 code (sign bit 3, magnitude index bits 2..0) of
+// the value as the quantisers encode it, and the UE4M3 byte of the value as a block
+// scale is encoded (meaningful for non-negative values).
+__global__ void selftest_codecs_kernel(uint32_t first, int64_t n, uint8_t* e2m1, uint8_t* e4m3) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float f = __uint_as_float(first + (uint32_t)i);
+    e2m1[i] = (uint8_t)(e2m1x2(f, 0.0f) & 0xFu);
+    e4m3[i] = (uint8_t)e4m3_byte(f);
+  }
+}
+
+moe_status selftest_codecs(uint32_t first, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t st) {
+  if (n == 0) return MOE_OK;
+  selftest_codecs_kernel<<<num_sms() * 8, 256, 0, st>>>(first, n, e2m1, e4m3);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -87,6 +87,10 @@ def test_argument_checks_fail_before_any_device_work(B):
                                    null, null, null, null, null, null, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_cast_output(null, null, 4, 7, null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_selftest_bounded_wait(null, null, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_codecs(0, 16, null, null, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_codecs(0, -1, null, null, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_codecs(0xFFFFFFF0, 17, 8, 8, null) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_codecs(0, 0, null, null, null) == B.MOE_OK
     assert lib.moe_quantize_weights(null, null, 2, 128, 256, null, null, null, null, null, null, null, null, 0,
                                     null) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_fold_gate_up_scales(null, null, null, null, 2, 128, 256, null) == B.MOE_ERR_INVALID_ARG
