@@ -37,6 +37,10 @@
 // Tiles are (expert, n-tile, pair of 128-row m-tiles), m fastest, dealt round-robin
 // over the pairs.  An expert with an odd number of m-tiles leaves the peer's half of
 // its last tile empty: the peer loads no A rows there and stores nothing.
+// Teardown: a CTA leaves only after every arrival aimed at its barriers has landed,
+// including the ones nobody consumes in the pipeline (the multicast release of each
+// stage's last use, the last tile's remote tempty arrivals): its producer and the
+// leader's MMA thread wait for those phases before the final cluster barrier.
 #include <algorithm>
 
 #include "gemm_tiled.cuh"
@@ -191,6 +195,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 200000ull) {
         }
+      } else {
+        // The release of each stage's last use is a multicast commit from the leader's
+        // MMA thread that nobody else waits for; it must land in this CTA's empty[i]
+        // before the CTA (and its shared memory) is gone.
+        for (int i = 0; i < kPStages; ++i)
+          if (issued[i] && !wait_bar_bounded(&s.empty[i], issued_phase[i], abort_flag, p.status)) break;
       }
     }
   } else if (warp == 1) {
@@ -219,6 +229,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         tc_commit_pair_mc(&s.tfull, 0x3);
       }
+      // the last tile's 16 epilogue arrivals (8 of them remote, from the peer) land here
+      // before this CTA can leave
+      if (ok && it > 0) wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status);
       // all MMAs issued by this thread complete before TMEM is released
       tc_commit_pair_mc(&s.drain, 0x1);
       wait_bar_drain(&s.drain, 0);

@@ -134,6 +134,46 @@ def test_forward_graph_capture_and_replay():
     assert_layer_close(got, eager.float().cpu().numpy(), "graph vs eager")
 
 
+@pytest.mark.parametrize("mode", ["dynamic", "fixed"])
+def test_forward_many_pairs_scatter_path(mode):
+    """More routed pairs than the fused prologue routes (8192): the chunked routing
+    kernels and the separate amax kernel run, while the output is small enough for the
+    fp32 scatter epilogue.  Experts own 2-3 m-tiles, so most end on a 256-row tile whose
+    second half is empty and whose first half is sparse.  The call is then captured
+    and replayed many times, L2 flushed in between, each replay checked."""
+    wl = workloads.small("many_pairs", T=1100, K=256, I=128, E=32, topk=8)
+    assert wl.T * wl.topk > 8192
+    W = oracle_weights(wl)
+    gs_h = None if mode == "dynamic" else workloads.fixed_gs_h(wl)
+    layer = _layer(W, wl)
+    fw = R.Forward(layer, wl.T, B.MOE_GS_DYNAMIC if mode == "dynamic" else B.MOE_GS_FIXED)
+    if gs_h is not None:
+        fw.gs_h.fill_(float(gs_h))
+    x = workloads.activations(wl)
+    ids, w = workloads.routing(wl)
+    ref = omoe.forward(x.float().numpy(), ids, w, wl.E, wl.expert_offset, W, gs_h=gs_h)["out"]
+    xd, ids_d, w_d = x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fw(xd, ids_d, w_d, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert fw.status.item() == 0
+    assert_layer_close(fw.out.float().cpu().numpy(), ref, "eager")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fw(xd, ids_d, w_d)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    for i in range(40):
+        flush.sum()
+        g.replay()
+        if i % 8 == 7:
+            torch.cuda.synchronize()
+            assert fw.status.item() == 0
+            assert_layer_close(fw.out.float().cpu().numpy(), ref, f"replay {i}")
+
+
 def test_simulated_expert_parallel_sum():
     """Ranks r = 0..3 each run their 6 local experts of 24 global ones on one
     GPU, one after another; the sum of their outputs matches the oracle layer
