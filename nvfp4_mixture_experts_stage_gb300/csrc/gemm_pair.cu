@@ -21,16 +21,19 @@
 //                      the B atoms of all 256 weight rows: the MMA reads every B scale
 //                      from the local TMEM), then its A rows and its 128 weight rows, into
 //                      a five-stage ring.  The loads use the CTA-pair form of TMA, so the
-//                      peer's bytes count directly on the leader's sf_full[s] (scales) and
+//                      peer's bytes count directly on the leader's sf_full[c][s] (scales) and
 //                      full[s] (operands); the leader's producer arms both with the bytes
 //                      of the two CTAs.
 //   warp 1, leader     MMA issuer: four M=256 N=256 K=64 MMAs per stage once full[s]
 //                      completes (operand bytes of both CTAs + the copier's commit); a
 //                      multicast commit frees the stage in both CTAs; a multicast commit
 //                      on tfull hands the accumulator to both epilogues.
-//   warps 2, 3, leader scale copiers, alternating stages: once sf_full[s] completes, the
-//                      stage's 12 scale atoms into both TMEMs (one cta_group::2 copy each),
-//                      then a commit on full[s].
+//   warps 2, 3, leader scale copiers, alternating stages (copier c takes the stages g
+//                      with g % 2 == c): once sf_full[c][s] completes, the stage's 12 scale
+//                      atoms into both TMEMs (one cta_group::2 copy each), then a commit on
+//                      full[s].  Each copier has its own sf_full barriers: a barrier whose
+//                      consecutive phases were waited on by different warps could let one
+//                      of them, two uses ahead, pass on the parity of an older phase.
 //   warps 4-11 (both)  epilogue of this CTA's 128 rows (shared with the single-CTA
 //                      kernel); after reading the accumulator every warp arrives on the
 //                      leader's tempty (16 arrivals), which the next tile's MMAs wait for.
@@ -65,7 +68,7 @@ struct __align__(1024) PairSmem {
   uint8_t b[kPStages][kPBStage];
   uint8_t sfa[kPStages][kPSfaStage];
   uint8_t sfb[kPStages][kPSfbStage];
-  uint64_t sf_full[kPStages];  // leader: both CTAs' scale atoms of the stage have landed
+  uint64_t sf_full[2][kPStages];  // leader, per copier: both CTAs' scale atoms of the stage have landed
   uint64_t full[kPStages];     // leader: both CTAs' operands landed and the scales are in TMEM
   uint64_t empty[kPStages];    // the pair's MMAs of the stage are done (multicast commit)
   uint64_t tfull;            // accumulator complete (multicast commit)
@@ -103,7 +106,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   build_tile_table(s, p, 2);
   if (threadIdx.x == 32) {
     for (int i = 0; i < kPStages; ++i) {
-      mbar_init(&s.sf_full[i], 1);
+      mbar_init(&s.sf_full[0][i], 1);
+      mbar_init(&s.sf_full[1][i], 1);
       mbar_init(&s.full[i], 2);  // the producer's arming + the copier's commit (+ the bytes)
       mbar_init(&s.empty[i], 1);
     }
@@ -144,7 +148,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int i = 0; i < kPStages; ++i) issued[i] = false;
       bool ok = true;
       TileCursor cur;
-      const uint32_t sf_full0 = mapa_shared(smem_u32(&s.sf_full[0]), 0);
+      const uint32_t sf_full0[2] = {mapa_shared(smem_u32(&s.sf_full[0][0]), 0),
+                                    mapa_shared(smem_u32(&s.sf_full[1][0]), 0)};
+      uint32_t g = 0;  // stages issued so far; stage g's scales go to copier g % 2
       const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);
       for (int t = pair; t < total_tiles && ok; t += npairs) {
         int n, mp;
@@ -163,10 +169,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (rank == 0) {
             // both CTAs' bytes: SFA 2 KB + SFB 4 KB each (A rows only where the CTA has rows);
             // A 16 KB + B 16 KB each
-            mbar_arrive_expect_tx(&s.sf_full[stage], 2 * 4096 + 2048 * (1 + (peer_rows ? 1 : 0)));
+            mbar_arrive_expect_tx(&s.sf_full[g & 1][stage], 2 * 4096 + 2048 * (1 + (peer_rows ? 1 : 0)));
             mbar_arrive_expect_tx(&s.full[stage], 2 * kPBStage + kPAStage * (1 + (peer_rows ? 1 : 0)));
           }
-          const uint32_t sfb = sf_full0 + 8 * stage, fb = full0 + 8 * stage;
+          const uint32_t sfb = sf_full0[g & 1] + 8 * stage, fb = full0 + 8 * stage;
           const int x = kb * kBKBytes;
           if (has_rows) tma_load_2d_pair(s.sfa[stage], &tmap_sfa, sfb, 0, sfa_row + 8 * kb);
 #pragma unroll
@@ -183,6 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
           issued[stage] = true;
           issued_phase[stage] = phase;
+          ++g;
           if (++stage == kPStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -239,15 +246,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else if (warp <= 3) {
     // ------------------------------------------------------------ scale copiers (leader)
     // copier c takes stages c, c + 2, ...: the A atom (column 4 kk) and the two B atoms
-    // (columns 16 + 8 kk and 16 + 8 kk + 4) of every k-step kk.
+    // (columns 16 + 8 kk and 16 + 8 kk + 4) of every k-step kk.  kPStages is odd, so
+    // these are the uses of sf_full[c][s] in order, one phase each.
     if (rank == 0 && lane == 0) {
       const uint64_t dsa0 = sdesc_sf(s.sfa[0]), dsb0 = sdesc_sf(s.sfb[0]);
-      for (int g = warp - 2; g < my_stages; g += 2) {
+      const int c = warp - 2;
+      for (int g = c; g < my_stages; g += 2) {
         const int kb = g % nkb;
         const int natoms = min(4, ksf4 - 4 * kb);
         const int stage = g % kPStages;
-        const uint32_t phase = (uint32_t)(g / kPStages) & 1;
-        if (!wait_bar_bounded(&s.sf_full[stage], phase, abort_flag, p.status)) break;
+        // this copier's uses of stage s are g = g0, g0 + 2 * kPStages, ...: use g / 10
+        const uint32_t phase = (uint32_t)(g / (2 * kPStages)) & 1;
+        if (!wait_bar_bounded(&s.sf_full[c][stage], phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t sf = tmem + kPSfBase + stage * kPSfCols;
         const uint64_t dsa = dsa0 + (uint64_t)((stage * kPSfaStage) >> 4);

@@ -18,7 +18,12 @@
 //     memory while the current chunk runs;
 //   * two MMA-issuing warps split every tile's k-blocks by parity into two
 //     accumulators (the epilogue adds them), since the tensor pipe serves each
-//     issuing thread at about one instruction per ~130 cycles.
+//     issuing thread at about one instruction per ~130 cycles.  Only when a tile
+//     has an even number of k-blocks: then every ring stage always belongs to the
+//     same issuer.  With an odd count the stages would alternate between the two,
+//     and a barrier whose consecutive phases are waited on by different threads can
+//     let one of them, two uses ahead, pass on the parity of an older phase; one
+//     issuer then takes all k-blocks.
 //
 // Scale-factor placement read by kind::mxf4nvf4.block_scale.scale_vec::4X (M=128):
 // operand A row m at TMEM lane m, column base + m/32; operand B row n at lane n%32,
@@ -213,6 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_hi = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
   const int nkb = (p.Kred + 255) >> 8;
   const int ksf4 = p.Kred >> 6;  // k-steps (scale atoms per 128 rows)
+  // both issuers take k-blocks only when a tile has an even number of them (with the
+  // even ring length, each stage then always has the same issuer)
+  const bool two_issuers = nkb % 2 == 0;
+  static_assert(Cfg<CHUNK>::kStages % 2 == 0, "stages alternate between issuers");
   int* abort_flag = &s.abort_flag;
 
   if (warp == 0) {
@@ -287,8 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Two threads issue concurrently (the tensor pipe serves each issuing thread at
     // roughly one instruction per ~130 cycles): issuer r takes the k-blocks with
     // kb % 2 == r of every tile and accumulates into its own 64 columns; the
-    // epilogue adds the two partial sums.  Each issuer copies the resident
-    // activation scales of its own k-blocks during the first tile of a chunk.
+    // epilogue adds the two partial sums.  With an odd number of k-blocks per tile
+    // issuer 0 takes them all and issuer 1 only keeps the per-tile and per-chunk
+    // commits.  Each issuer copies the resident activation scales of its own
+    // k-blocks during the first tile of a chunk.
     if (lane == 0) {
       const int r = warp == 1 ? 0 : 1;
       bool ok = true;
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + (2 * buf + r) * kChunk;
         bool first = true;
-        for (int kb = r; kb < nkb; kb += 2) {
+        for (int kb = two_issuers ? r : (r == 0 ? 0 : nkb); kb < nkb; kb += two_issuers ? 2 : 1) {
           const uint32_t gs = g + kb;
           const int stage = gs % kStages;
           const uint32_t phase = (gs / kStages) & 1;
@@ -432,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float v[kChunk];
 #pragma unroll
       for (int j = 0; j < kChunk; j += 16) tmem_ld16(taddr + j, *reinterpret_cast<float(*)[16]>(&v[j]));
-      if (nkb > 1) {  // partial sum of the odd k-blocks
+      if (two_issuers) {  // partial sum of the odd k-blocks
 #pragma unroll
         for (int j = 0; j < kChunk; j += 16) {
           float y[16];

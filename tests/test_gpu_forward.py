@@ -58,6 +58,8 @@ SMALL = [
     workloads.small("ragged", T=77, K=384, I=192, E=5, topk=2, routing="softmax_topk", x_kind="outliers"),
     workloads.small("top1", T=300, K=256, I=128, E=4, topk=1),
     workloads.small("bigrows", T=130, K=256, I=64, E=3, topk=2, x_kind="big_rows"),
+    # three 256-deep k-blocks per tile in both GEMMs (an odd count)
+    workloads.small("odd_kblocks", T=96, K=768, I=768, E=4, topk=2),
 ]
 
 
