@@ -148,8 +148,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       for (int i = 0; i < kPStages; ++i) issued[i] = false;
       bool ok = true;
       TileCursor cur;
-      const uint32_t sf_full0[2] = {mapa_shared(smem_u32(&s.sf_full[0][0]), 0),
-                                    mapa_shared(smem_u32(&s.sf_full[1][0]), 0)};
+      // leader addresses of the two copiers' sf_full rings (scalars: a runtime-indexed
+      // array would live in local memory and cost a load on every stage)
+      const uint32_t sf_full_c0 = mapa_shared(smem_u32(&s.sf_full[0][0]), 0);
+      const uint32_t sf_full_c1 = mapa_shared(smem_u32(&s.sf_full[1][0]), 0);
       uint32_t g = 0;  // stages issued so far; stage g's scales go to copier g % 2
       const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);
       for (int t = pair; t < total_tiles && ok; t += npairs) {
@@ -172,7 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             mbar_arrive_expect_tx(&s.sf_full[g & 1][stage], 2 * 4096 + 2048 * (1 + (peer_rows ? 1 : 0)));
             mbar_arrive_expect_tx(&s.full[stage], 2 * kPBStage + kPAStage * (1 + (peer_rows ? 1 : 0)));
           }
-          const uint32_t sfb = sf_full0[g & 1] + 8 * stage, fb = full0 + 8 * stage;
+          const uint32_t sfb = ((g & 1) ? sf_full_c1 : sf_full_c0) + 8 * stage, fb = full0 + 8 * stage;
           const int x = kb * kBKBytes;
           if (has_rows) tma_load_2d_pair(s.sfa[stage], &tmap_sfa, sfb, 0, sfa_row + 8 * kb);
 #pragma unroll
