@@ -42,7 +42,7 @@ METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 
 NCU_TRAFFIC = {
     ("decode", "auto", "gemm_l1"): {
         "bytes": 673994496,
-        "kernel_sources": ("gemm_stream.cu", "tcgen05.cuh", "common.cuh"),
+        "kernel_sources": ("gemm_stream.cu", "pipeline.cuh", "tcgen05.cuh", "common.cuh"),
         "sources_sha256_16": "e2703825511dc62a",
     },
 }

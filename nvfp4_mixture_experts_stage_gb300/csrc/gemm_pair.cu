@@ -47,6 +47,7 @@
 #include <algorithm>
 
 #include "gemm_tiled.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 
@@ -152,7 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // array would live in local memory and cost a load on every stage)
       const uint32_t sf_full_c0 = mapa_shared(smem_u32(&s.sf_full[0][0]), 0);
       const uint32_t sf_full_c1 = mapa_shared(smem_u32(&s.sf_full[1][0]), 0);
-      uint32_t g = 0;  // stages issued so far; stage g's scales go to copier g % 2
+      uint32_t g = 0;  // stages issued so far; stage g's scales go to copier sched::pair_copier(g)
       const uint32_t full0 = mapa_shared(smem_u32(&s.full[0]), 0);
       for (int t = pair; t < total_tiles && ok; t += npairs) {
         int n, mp;
@@ -171,10 +172,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (rank == 0) {
             // both CTAs' bytes: SFA 2 KB + SFB 4 KB each (A rows only where the CTA has rows);
             // A 16 KB + B 16 KB each
-            mbar_arrive_expect_tx(&s.sf_full[g & 1][stage], 2 * 4096 + 2048 * (1 + (peer_rows ? 1 : 0)));
+            mbar_arrive_expect_tx(&s.sf_full[sched::pair_copier(g)][stage],
+                                  2 * 4096 + 2048 * (1 + (peer_rows ? 1 : 0)));
             mbar_arrive_expect_tx(&s.full[stage], 2 * kPBStage + kPAStage * (1 + (peer_rows ? 1 : 0)));
           }
-          const uint32_t sfb = ((g & 1) ? sf_full_c1 : sf_full_c0) + 8 * stage, fb = full0 + 8 * stage;
+          const uint32_t sfb = (sched::pair_copier(g) ? sf_full_c1 : sf_full_c0) + 8 * stage,
+                         fb = full0 + 8 * stage;
           const int x = kb * kBKBytes;
           if (has_rows) tma_load_2d_pair(s.sfa[stage], &tmap_sfa, sfb, 0, sfa_row + 8 * kb);
 #pragma unroll
@@ -253,12 +256,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (rank == 0 && lane == 0) {
       const uint64_t dsa0 = sdesc_sf(s.sfa[0]), dsb0 = sdesc_sf(s.sfb[0]);
       const int c = warp - 2;
-      for (int g = c; g < my_stages; g += 2) {
+      for (int g = c; g < my_stages; g += 2) {  // the stages with sched::pair_copier(g) == c
         const int kb = g % nkb;
         const int natoms = min(4, ksf4 - 4 * kb);
-        const int stage = g % kPStages;
-        // this copier's uses of stage s are g = g0, g0 + 2 * kPStages, ...: use g / 10
-        const uint32_t phase = (uint32_t)(g / (2 * kPStages)) & 1;
+        const int stage = (int)sched::pair_stage((uint32_t)g, kPStages);
+        const uint32_t phase = sched::pair_sf_use((uint32_t)g, kPStages) & 1;
         if (!wait_bar_bounded(&s.sf_full[c][stage], phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t sf = tmem + kPSfBase + stage * kPSfCols;

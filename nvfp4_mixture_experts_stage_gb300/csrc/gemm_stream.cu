@@ -31,6 +31,7 @@
 // tcgen05.cp.32x128b.warpx4 satisfies the A placement directly; the B images put
 // the chunk's rows i and 32+i in bytes 0..3 and 4..7 of image row i.
 #include "tcgen05.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 namespace stream {
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ksf4 = p.Kred >> 6;  // k-steps (scale atoms per 128 rows)
   // both issuers take k-blocks only when a tile has an even number of them (with the
   // even ring length, each stage then always has the same issuer)
-  const bool two_issuers = nkb % 2 == 0;
+  const bool two_issuers = sched::stream_two_issuers(nkb);
   static_assert(Cfg<CHUNK>::kStages % 2 == 0, "stages alternate between issuers");
   int* abort_flag = &s.abort_flag;
 
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + (2 * buf + r) * kChunk;
         bool first = true;
-        for (int kb = two_issuers ? r : (r == 0 ? 0 : nkb); kb < nkb; kb += two_issuers ? 2 : 1) {
+        for (int kb = sched::stream_first_kb(r, nkb); kb < nkb; kb += sched::stream_kb_step(nkb)) {
           const uint32_t gs = g + kb;
           const int stage = gs % kStages;
           const uint32_t phase = (gs / kStages) & 1;
