@@ -118,3 +118,17 @@ def test_bench_traffic_is_keyed_by_workload_policy_and_kernel_sources():
     finally:
         tr.clear()
         tr.update(saved)
+
+
+def test_bench_rejects_throttled_or_locked_clocks():
+    """A timed region is re-measured once if its clock samples saw a hardware or thermal
+    slowdown, or SM clocks well below their maximum with no reason (a leftover lock);
+    the power cap alone is kept."""
+    import bench
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected({**ok, "sm_mhz": 1900.0, "reasons": ["sw_power_cap"]})
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected({**ok, "reasons": [r]})
+    assert bench.clocks_rejected({**ok, "sm_mhz": 1000.0})
+    assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]})
