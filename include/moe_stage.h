@@ -21,6 +21,11 @@
  *    noted (BF16 tensors: 16 bytes).
  *  - Work is enqueued on the caller's stream, never synchronises the host, and
  *    can be captured into a CUDA graph (no host reads of device data).
+ *  - Devices: the library looks up launch settings (the SM count, the kernels'
+ *    shared-memory limits, the CTA-pair kernel's grid) on its first launch in the
+ *    process and reuses them, so a process drives one device (one process per GPU,
+ *    the current device at the first call).  Make the first call of each entry point
+ *    outside stream capture.
  *  - Return value: MOE_OK, or an error found on the host before anything was
  *    enqueued (MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE),
  *    or MOE_ERR_CUDA if a launch failed.
