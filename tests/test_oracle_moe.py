@@ -317,3 +317,33 @@ def test_fold_gives_one_alpha_l1_close_to_two_alphas():
         a, b = a[valid].astype(np.float64), b[valid].astype(np.float64)
         assert np.abs(a - b).max() <= 0.1 * np.abs(b).max()
         assert float((a * b).sum() / np.sqrt((a * a).sum() * (b * b).sum())) > 0.99
+
+
+def test_quantize_weights_gate_up_split_scales_and_error_bound():
+    """oracle.moe.quantize_weights against closed forms: the gate rows (0..I-1), the up
+    rows (I..2I-1) and each down projection get their own global scale amax / 2688
+    (fp32 division), scales are row-major [N, K/16], and every dequantised weight q is
+    within s * gs of the weight w, s its decoded block scale: in scaled units the error
+    is at most half the widest gap of the E2M1 grid (4 to 6), or the overshoot past 6
+    when the block scale rounded down (under 0.4)."""
+    r = np.random.default_rng(21)
+    E, I, K = 3, 32, 64
+    w1 = q.bf16_round(r.standard_normal((E, 2 * I, K)).astype(F32) * 0.02)
+    w1[:, :I] *= F32(50.0)                       # gate rows far larger than up rows
+    w1 = q.bf16_round(w1)
+    w2 = q.bf16_round(r.standard_normal((E, K, I)).astype(F32) * 0.03)
+    W = moe.quantize_weights(w1, w2)
+    assert W["w1_codes"].shape == (E, 2 * I, K // 2) and W["w1_sf"].shape == (E, 2 * I, K // 16)
+    assert W["w2_codes"].shape == (E, K, I // 2) and W["w2_sf"].shape == (E, K, I // 16)
+    for e in range(E):
+        halves = ((slice(0, I), W["gs_w1_gate"][e]), (slice(I, 2 * I), W["gs_w1_up"][e]))
+        for rows, gs in halves:
+            assert gs == F32(np.abs(w1[e, rows]).max()) / F32(2688.0)
+            deq = q.dequantize(W["w1_codes"][e, rows], W["w1_sf"][e, rows]) * float(gs)
+            step = np.repeat(q.e4m3_decode(W["w1_sf"][e, rows]).astype(np.float64), 16, axis=1) * float(gs)
+            assert np.all(np.abs(w1[e, rows] - deq) <= step * (1 + 1e-6))
+        assert W["gs_w2"][e] == F32(np.abs(w2[e]).max()) / F32(2688.0)
+        deq2 = q.dequantize(W["w2_codes"][e], W["w2_sf"][e]) * float(W["gs_w2"][e])
+        step2 = np.repeat(q.e4m3_decode(W["w2_sf"][e]).astype(np.float64), 16, axis=1) * float(W["gs_w2"][e])
+        assert np.all(np.abs(w2[e] - deq2) <= step2 * (1 + 1e-6))
+    assert np.all(W["gs_w1_gate"] > 20 * W["gs_w1_up"])
