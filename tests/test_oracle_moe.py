@@ -244,6 +244,66 @@ def test_bf16_reference_layer_brute_force_and_close_to_nvfp4():
     assert cos > 0.95   # 0.975 here: the tiny inputs carry 1 % outliers at 20x
 
 
+def test_bf16_reference_layer_closed_form():
+    """forward_bf16 on a hand-built layer whose every intermediate is known exactly, so
+    each BF16 rounding point of the pages' pipeline ([tests] "complete pipeline": L1 out
+    g and u in BF16, SiLU(g) * up in BF16, L2 out in BF16, the weighted sum in BF16) and
+    the gate/up split show in the output.  One token, x = e_0 (so g and u are column 0
+    of the gate and up rows), two local experts with routing weights 1 and 0.5.
+
+    Expert 0 (gate, up) in column 0, by row i of h:
+      i=0: (128.75, 1.5)         g = bf16(128.75) = 129 (spacing 1 on [128, 256));
+                                 silu(129) = 129 exactly in fp32 (exp(-129) underflows);
+                                 h = bf16(193.5) = 194 (tie -> even mantissa)
+      i=1: (192, 1.005859375)    u = bf16(1 + 3/512) = 1.0078125; h = bf16(193.5) = 194
+      i=2: (0, 5)                silu(0) = 0 -> h = 0
+      i=3: (-192, 5)             exp(192) overflows fp32: silu = -192/inf = -0 -> h = 0
+      i=4: (128, 1)              h = 128
+      i=5: (1, 1)                silu(1) = 1/(1 + e^-1) = 0.7310586 -> h = bf16 = 0.73046875
+                                 (187.15 steps of 2^-8, far from a rounding midpoint)
+    Expert 0 down rows (output column k: weights on h):
+      k=0: 1*h0                  -> 194
+      k=1: 1*h0 + 2^-9*h1        -> bf16(194.37890625) = 194
+      k=2: 1*h0 - 1.5078125*h4   -> 194 - 193 = 1
+      k=3: 1*h1 - 1.5078125*h4   -> 1
+      k=4: 1*h2 + 1*h3           -> 0
+      k=5: 1*h5                  -> 0.73046875
+    Expert 1: gate/up (128, 1) in row 0 -> h'0 = 128; down row k=1: 0.005859375*h'0 = 0.75.
+    out = bf16(1*y0 + 0.5*y1), in fp32: k=1 gives bf16(194 + 0.375) = 194; the rest as y0.
+
+    A missing rounding of g gives 193 in column 0 (h0 = bf16(128.75*1.5) = 193); of u gives
+    0 in column 3 (h1 = 193); of h gives 0.5 in column 2; of y gives 195 in column 1
+    (194.3789 + 0.375); of the output gives 194.375 in column 1; gate and up swapped give
+    other values in column 0; a sign error in SiLU gives -960 in column 4."""
+    K, I, E = 16, 16, 2
+    x = np.zeros((1, K), F32)
+    x[0, 0] = 1.0
+    w1 = np.zeros((E, 2 * I, K), F32)
+    w2 = np.zeros((E, K, I), F32)
+    for i, (g, u) in enumerate([(128.75, 1.5), (192.0, 1.005859375), (0.0, 5.0), (-192.0, 5.0), (128.0, 1.0),
+                                (1.0, 1.0)]):
+        w1[0, i, 0], w1[0, I + i, 0] = g, u
+    w2[0, 0, 0] = 1.0
+    w2[0, 1, 0], w2[0, 1, 1] = 1.0, 2.0 ** -9
+    w2[0, 2, 0], w2[0, 2, 4] = 1.0, -1.5078125
+    w2[0, 3, 1], w2[0, 3, 4] = 1.0, -1.5078125
+    w2[0, 4, 2], w2[0, 4, 3] = 1.0, 1.0
+    w2[0, 5, 5] = 1.0
+    w1[1, 0, 0], w1[1, I, 0] = 128.0, 1.0
+    w2[1, 1, 0] = 0.005859375
+    ids = np.array([[0, 1]], np.int32)
+    wts = np.array([[1.0, 0.5]], F32)
+    out = moe.forward_bf16(x, ids, wts, E, 0, lambda e: w1[e], lambda e: w2[e])
+    expect = np.zeros(K, F32)
+    expect[:6] = [194.0, 194.0, 1.0, 1.0, 0.0, 0.73046875]
+    assert out.shape == (1, K)
+    assert np.array_equal(out[0], expect), out[0]
+    # tokens routed to no local expert (foreign id, -1) give exactly zero
+    out2 = moe.forward_bf16(np.concatenate([x, x]), np.array([[0, 1], [5, -1]], np.int32),
+                            np.concatenate([wts, wts]), E, 0, lambda e: w1[e], lambda e: w2[e])
+    assert np.array_equal(out2[0], expect) and not out2[1].any()
+
+
 # ------------------------------------------------------------- gate/up scale fold
 def _nearest_e4m3_brute(v):
     """Nearest UE4M3 byte to v >= 0 by search over every finite byte (torch's float8

@@ -10,14 +10,19 @@ from oracle import nvfp4 as q
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
+def _num(tok):
+    """A decimal or hex-float (0x1p-130) literal."""
+    return float.fromhex(tok) if "0x" in tok else float(tok)
+
+
 def _golden_blocks():
     out = []
     for line in open(os.path.join(GOLDEN, "quant_blocks.txt")):
         if not line.strip() or line.startswith("#"):
             continue
         name, gs, xs, sb, nibs, bts = [f.strip() for f in line.split("|")]
-        out.append((name, None if gs == "data" else float(gs),
-                    np.array([float(v) for v in xs.split()], np.float32),
+        out.append((name, None if gs == "data" else _num(gs),
+                    np.array([_num(v) for v in xs.split()], np.float32),
                     int(sb, 16), [int(v) for v in nibs.split()],
                     [int(v, 16) for v in bts.split()]))
     return out
