@@ -3,16 +3,20 @@
 
 A step is one call of the whole layer (moe_forward: routing, global amax,
 quantisation into slots, L1 grouped GEMM with the fused SiLU*up + requant
-epilogue, L2 grouped GEMM with the fused weighted scatter, output cast) over
-one batch of the decode-size workload: T=256 tokens, hidden 4096,
-intermediate 3072, 48 local experts of 384 (rank 3), top-8 uniform routing,
-BF16 N(0,1) activations and NVFP4 weights quantised from N(0, 0.02) (seeded
-synthetic data; no checkpoint).  The h global scale is calibrated once in the
+epilogue, L2 grouped GEMM, weighted combine into the BF16 output) over one batch
+of the prefill-size workload: T=8192 tokens, hidden 4096, intermediate 3072, 48
+local experts, top-8 uniform routing (65,536 slots), BF16 N(0,1) activations
+with rows of amax up to 1e4, NVFP4 weights quantised from N(0, 0.02) (seeded
+synthetic data; no checkpoint).  This is the largest single-GPU layer
+configuration and the tensor-bound one, so the line reports the grouped GEMMs
+against the dense FP4 tensor peak.  The h global scale is calibrated once in the
 warm-up (the data-derived scale of a first call) and then held fixed, the
 inference mode of the vllm/nvfp4_cutedsl.py commit pages; x's global scale is
-recomputed every step.
+recomputed every step.  The other workloads (decode, skewed routing, the
+quantise/route bandwidth sweep) are reported under "configs".
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--study]
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 of the workload (weak scaling: the layer does not shard across GPUs here).
 """
@@ -36,9 +40,9 @@ import workloads  # noqa: E402
 
 METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 peak"
 
-# DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture
-# (profiles/gemm_l1_stream_decode.md), keyed by (workload, GEMM policy, stage) and valid
-# only while the files that kernel is compiled from hash to the captured ones.
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture of
+# the same workload, keyed by (workload, GEMM policy, stage) and valid only while the
+# files that kernel is compiled from hash to the captured ones.
 NCU_TRAFFIC = {
     ("decode", "auto", "gemm_l1"): {
         "bytes": 673994496,
@@ -73,7 +77,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="prefill")
+    ap.add_argument("--study", action="store_true",
+                    help="also run the accuracy comparisons against the BF16 layer (not timed; slow)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other workloads of the table (prefill, skewed routing) after the headline")
@@ -356,6 +362,18 @@ def e2e_steps(fw, x_h, ids_h, w_h, x, ids, w, out_h, steps, warmup, ws):
     return res[0], res[1]
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return None
+
+
 def cpu_baseline_oracle(wl, x, ids, w, n_tokens):
     """The CPU oracle on a bounded sample of the same workload: the layer for
     the first n_tokens tokens (their own batch), weights of the experts they
@@ -379,6 +397,47 @@ def cpu_baseline_oracle(wl, x, ids, w, n_tokens):
     omoe.forward(xs, ids_s, w_s, E, wl.expert_offset, W)
     dt = time.perf_counter() - t0
     return n_tokens / dt, dt, len(touched)
+
+
+_SINGLE_THREAD_SCRIPT = r"""
+import json, sys, time
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+import workloads
+from oracle import moe as omoe, nvfp4 as oq
+from oracle.route import route as oroute
+res = {}
+wl = workloads.WORKLOADS["tiny"]
+x = workloads.activations(wl).float().numpy()
+ids, w = workloads.routing(wl)
+W = omoe.quantize_weights(np.stack([workloads.expert_w1(wl, e).float().numpy() for e in range(wl.E)]),
+                          np.stack([workloads.expert_w2(wl, e).float().numpy() for e in range(wl.E)]))
+t0 = time.perf_counter(); n = 0
+while time.perf_counter() - t0 < 2.0:
+    omoe.forward(x, ids, w, wl.E, wl.expert_offset, W); n += 1
+res["tiny_layer_tokens_per_s"] = wl.T * n / (time.perf_counter() - t0)
+sw = workloads.WORKLOADS["sweep_1k"]
+xs = workloads.activations(sw).float().numpy()
+t0 = time.perf_counter(); oq.quantize(xs); dt = time.perf_counter() - t0
+res["sweep_1k_quantize_gbs"] = (xs.size * 2 + xs.size // 2 + xs.size // 16) / dt / 1e9
+ids, w = workloads.routing(sw)
+t0 = time.perf_counter(); oroute(ids, w, sw.E, sw.expert_offset); dt = time.perf_counter() - t0
+res["sweep_1k_route_gbs"] = ids.size * 20 / dt / 1e9
+print(json.dumps(res))
+"""
+
+
+def cpu_single_thread():
+    """The oracle with one host thread (BLAS and OpenMP pinned to one thread in a child
+    process) on the tiny layer and the 1k-token quantise/route sweep."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, "-c", _SINGLE_THREAD_SCRIPT, ROOT], capture_output=True, text=True,
+                           timeout=300, env=env)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else {"error": r.stderr[-300:]}
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"error": str(e)}
 
 
 def run_ours(args, ws, rank, local):
@@ -416,10 +475,11 @@ def run_ours(args, ws, rank, local):
     cal(x, ids, w)
     torch.cuda.synchronize()
     gs_h_cal = float(cal.gs_h.item())
+    del cal
     fw = R.Forward(layer, wl.T, B.MOE_GS_FIXED)
     fw.gs_h.fill_(gs_h_cal)
 
-    # bookkeeping for the algorithmic byte count (not part of the timed path)
+    # bookkeeping for the algorithmic byte and flop counts (not part of the timed path)
     loc = ids_np.reshape(-1).astype(np.int64) - wl.expert_offset
     counts = np.bincount(loc[(loc >= 0) & (loc < wl.E)], minlength=wl.E)
     alg = algorithmic(wl, counts)
@@ -440,27 +500,20 @@ def run_ours(args, ws, rank, local):
     if st != 0:
         raise RuntimeError(f"device status {st}: {B.moe_status_string(st)}")
 
-    # the data-derived (dynamic) h scale mode, same timing discipline
-    dyn_ms, dyn_stage, _ = timed_steps(cal, x, ids, w, max(3, args.steps // 2), 2, flush, ws)
-
     # end to end through the C ABI with host buffers
     x_h = x_c.pin_memory()
     ids_h = torch.from_numpy(ids_np).pin_memory()
     w_h = torch.from_numpy(w_np).pin_memory()
     out_h = torch.empty(wl.T, wl.K, dtype=torch.bfloat16).pin_memory()
     e2e_ms, e2e_serial_ms = e2e_steps(fw, x_h, ids_h, w_h, x, ids, w, out_h, args.steps, args.warmup, ws)
+    del x_h, out_h
 
     ms = max_over_ranks(float(step_ms.mean()), ws)
     e2e_ms = max_over_ranks(e2e_ms, ws)
     e2e_serial_ms = max_over_ranks(e2e_serial_ms, ws)
     pk = peaks()
     fp4_peak = pk["bf16_tflops"] * 6.0          # dense fp4 / bf16 = 13.5 / 2.25 (nominal ratio)
-    # dominant kernel of the step
-    dom = max(("gemm_l1", "gemm_l2"), key=lambda k: stage_ms[k])
-    dom_ms = stage_ms[dom]
-    dom_bytes = alg["l1_bytes"] if dom == "gemm_l1" else alg["l2_bytes"]
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload, args.gemm_policy, dom)
+    roof = layer_roofline(wl, alg, stage_ms, pk, fp4_peak, args.gemm_policy)
     gemm_ms = stage_ms["gemm_l1"] + stage_ms["gemm_l2"]
     gemm_tflops = (alg["flops_l1"] + alg["flops_l2"]) / (gemm_ms * 1e-3) / 1e12
 
@@ -477,12 +530,12 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e2m1 -> fp32 accumulate), bf16 activations",
         "data": "synthetic (seeded numpy PCG64; N(0,1) activations, N(0,0.02) weights quantised on the GPU)",
-        "config": {"workload": f"{wl.name}: T={wl.T}, K={wl.K}, I={wl.I}, E={wl.E} local of 384 (offset "
-                               f"{wl.expert_offset}), top-{wl.topk} uniform",
+        "config": {"workload": workload_desc(wl),
                    "tokens_per_step": wl.T, "local_slots": alg["S"], "experts_touched": alg["touched"],
                    "gs_h": "fixed (calibrated in warm-up)", "gs_x": "dynamic (amax every step)",
-                   "l2": "inputs larger than L2 (weights 1.02 GB streamed every step) and L2 flushed between timed steps by "
-                         "reading a 256 MB buffer (a read flush leaves no dirty lines to write back in the timed region)",
+                   "l2": "inputs larger than L2 (weights 1.02 GB streamed every step) and L2 flushed between timed "
+                         "steps by reading a 256 MB buffer (a read flush leaves no dirty lines to write back in the "
+                         "timed region)",
                    "launch": "each step one CUDA-graph replay of moe_forward (events at start and end only); "
                              "stage_ms from a second loop whose graph also records the stage boundaries",
                    "gemm_policy": args.gemm_policy,
@@ -490,14 +543,10 @@ def run_ours(args, ws, rank, local):
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "gemm_tflops": gemm_tflops,
         "gemm_frac_of_fp4_peak": gemm_tflops / fp4_peak,
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes": dom_bytes, "peak_source": pk["source"]},
-        "dynamic_gs_h": {"ms_per_step": float(dyn_ms.mean()), "value": wl.T / (float(dyn_ms.mean()) * 1e-3),
-                         "stage_ms": {k: round(v, 4) for k, v in dyn_stage.items()}},
+        "roofline": roof,
         "e2e": {"value": wl.T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4,
-                "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x_c.numel() * 2 + ids_np.size * 4 + w_np.size * 4,
+                "d2h_bytes_per_step": wl.T * wl.K * 2, "ms_per_step": e2e_ms,
                 "how": "moe_forward per step from pinned host buffers; copies on a second stream, "
                        "double-buffered, overlapping neighbouring steps",
                 "serial_ms_per_step": e2e_serial_ms},
@@ -505,19 +554,55 @@ def run_ours(args, ws, rank, local):
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if args.study and rank == 0:
         result["accuracy"] = accuracy_vs_bf16(wl, fw, x, ids, w, x_c, ids_np, w_np)
         result["weight_study"] = weight_study(wl, layer, fw, x, ids, w, x_c, ids_np, w_np, B, R)
+    del fw
+    torch.cuda.empty_cache()
     if not args.no_configs:
         result["configs"] = other_configs(wl, layer, fp4_peak, pk, flush, ws, R, B)
         result["configs"].update(sweep_configs(pk, B))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        n = 12
+        n = 12 if wl.n_global else 2     # about 10-20 s of oracle time either way
         v, dt, ne = cpu_baseline_oracle(wl, x_c, ids_np, w_np, n)
         result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                  "cpu": cpu_model(),
                                   "sample": f"first {n} tokens of the {wl.name} batch as their own batch "
-                                            f"({ne} experts touched), oracle forward, {dt:.1f} s"}
+                                            f"({ne} experts touched), oracle forward, {dt:.1f} s",
+                                  "single_thread": cpu_single_thread()}
     return result
+
+
+def workload_desc(wl):
+    routing = {"uniform": "uniform", "zipf_top1": "Zipf(1.2) top-1", "zipf_topk": "Zipf(1.2) Gumbel-top-k",
+               "softmax_topk": "softmax top-k"}[wl.routing]
+    glob = f" local of 384 (offset {wl.expert_offset})" if wl.n_global else " local"
+    return f"{wl.name}: T={wl.T}, K={wl.K}, I={wl.I}, E={wl.E}{glob}, top-{wl.topk} {routing}"
+
+
+def layer_roofline(wl, alg, stage_ms, pk, fp4_peak, policy):
+    """The roofline of the layer's dominant kernel (the slower grouped GEMM): the
+    tensor pipe (dense FP4) when its flops per algorithmic byte exceed the ridge,
+    HBM otherwise."""
+    dom = max(("gemm_l1", "gemm_l2"), key=lambda k: stage_ms[k])
+    dom_s = stage_ms[dom] * 1e-3
+    flops = alg["flops_l1"] if dom == "gemm_l1" else alg["flops_l2"]
+    nbytes = alg["l1_bytes"] if dom == "gemm_l1" else alg["l2_bytes"]
+    traffic = ncu_traffic(wl.name, policy, dom)
+    l1_tf = alg["flops_l1"] / (stage_ms["gemm_l1"] * 1e-3) / 1e12
+    l2_tf = alg["flops_l2"] / (stage_ms["gemm_l2"] * 1e-3) / 1e12
+    if flops / nbytes > fp4_peak * 1e12 / (pk["hbm_gbs"] * 1e9):
+        ach = flops / dom_s / 1e12
+        return {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": fp4_peak, "unit": "TFLOP/s",
+                "frac": ach / fp4_peak, "traffic": traffic, "algorithmic_flops": flops,
+                "algorithmic_bytes": nbytes,
+                "peak_source": pk["source"] + " bf16 burst x 6 (the nominal dense fp4/bf16 ratio)",
+                "l1_frac": l1_tf / fp4_peak, "l2_frac": l2_tf / fp4_peak,
+                "l1_tflops": l1_tf, "l2_tflops": l2_tf}
+    ach = nbytes / dom_s / 1e9
+    return {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / pk["hbm_gbs"], "traffic": traffic, "algorithmic_bytes": nbytes,
+            "peak_source": pk["source"]}
 
 
 def accuracy_vs_bf16(wl, fw, x, ids, w, x_c, ids_np, w_np, n_tokens=24):
@@ -636,13 +721,14 @@ def weight_study(wl, layer, fw, x, ids, w, x_c, ids_np, w_np, B, R, n_tokens=16)
 
 
 def other_configs(head, layer, fp4_peak, pk, flush, ws, R, B, steps=5, warmup=2):
-    """The tensor-bound workloads of the table on the same seeded experts: step time,
-    tokens/s and the grouped GEMMs' NVFP4 TFLOP/s as a fraction of the dense FP4 peak
-    (h scale fixed at its calibrated value; same timing discipline as the headline)."""
+    """The other layer workloads of the table on the same seeded experts: step time,
+    tokens/s, the grouped GEMMs' NVFP4 TFLOP/s as a fraction of the dense FP4 peak and
+    the dominant kernel's roofline (h scale fixed; same timing discipline as the
+    headline)."""
     out = {}
-    for name in ("prefill", "skew_top1", "skew_top8"):
+    for name in ("decode", "prefill", "skew_top1", "skew_top8"):
         wl = workloads.WORKLOADS[name]
-        if (wl.E, wl.K, wl.I, wl.seed) != (head.E, head.K, head.I, head.seed):
+        if name == head.name or (wl.E, wl.K, wl.I, wl.seed) != (head.E, head.K, head.I, head.seed):
             continue
         layer.topk, layer.expert_offset = wl.topk, wl.expert_offset
         x = workloads.activations(wl).cuda()
@@ -657,27 +743,14 @@ def other_configs(head, layer, fp4_peak, pk, flush, ws, R, B, steps=5, warmup=2)
         loc = ids_np.reshape(-1).astype(np.int64) - wl.expert_offset
         alg = algorithmic(wl, np.bincount(loc[(loc >= 0) & (loc < wl.E)], minlength=wl.E))
         ms = max_over_ranks(float(step_ms.mean()), ws)
-        l1_tf = alg["flops_l1"] / (stage_ms["gemm_l1"] * 1e-3) / 1e12
-        l2_tf = alg["flops_l2"] / (stage_ms["gemm_l2"] * 1e-3) / 1e12
         g_s = (stage_ms["gemm_l1"] + stage_ms["gemm_l2"]) * 1e-3
         g_tf = (alg["flops_l1"] + alg["flops_l2"]) / g_s / 1e12
-        g_bytes = alg["l1_bytes"] + alg["l2_bytes"]
-        # the roofline that binds: tensor above the ridge (flop per algorithmic byte), HBM below
-        tensor_bound = (alg["flops_l1"] + alg["flops_l2"]) / g_bytes > fp4_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
-        if tensor_bound:
-            roof = {"bound": "tensor", "achieved": g_tf, "peak": fp4_peak, "unit": "TFLOP/s", "frac": g_tf / fp4_peak,
-                    "peak_source": pk["source"] + " (bf16 x 6, the nominal fp4/bf16 ratio)",
-                    "l1_frac": l1_tf / fp4_peak, "l2_frac": l2_tf / fp4_peak}
-        else:
-            gbs = g_bytes / g_s / 1e9
-            roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"], "algorithmic_bytes": g_bytes}
         out[name] = {
-            "workload": f"{wl.name}: T={wl.T}, K={wl.K}, I={wl.I}, E={wl.E}, top-{wl.topk}",
+            "workload": workload_desc(wl),
             "ms_per_step": ms, "tokens_per_s": wl.T * ws / (ms * 1e-3), "local_slots": alg["S"],
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-            "gemm_l1_tflops": l1_tf, "gemm_l2_tflops": l2_tf, "gemm_tflops": g_tf,
-            "gemm_frac_of_fp4_peak": g_tf / fp4_peak, "roofline": roof,
+            "gemm_tflops": g_tf, "gemm_frac_of_fp4_peak": g_tf / fp4_peak,
+            "roofline": layer_roofline(wl, alg, stage_ms, pk, fp4_peak, "auto"),
         }
         del fw, x, ids, w
         torch.cuda.empty_cache()
@@ -686,8 +759,9 @@ def other_configs(head, layer, fp4_peak, pk, flush, ws, R, B, steps=5, warmup=2)
 
 
 def sweep_configs(pk, B, reps=20):
-    """moe_stage_activation (global amax, then block quantisation: two passes over x)
-    and moe_route alone on the bandwidth-sweep workloads, as HBM GB/s against the
+    """moe_stage_activation (global amax, then block quantisation: two passes over x),
+    moe_route alone, and the two as the layer runs them (routing, then quantisation
+    into the slots) on the bandwidth-sweep workloads, as HBM GB/s against the
     measured peak.  x rotates over buffers totalling more than twice L2, so every
     call starts from HBM; the quantiser's second read of x comes from L2 only when x
     itself fits there (algorithmic bytes count it once in that case)."""
@@ -753,6 +827,19 @@ def sweep_configs(pk, B, reps=20):
                                                     rbuf["pair_slot"], rws))
         r_bytes = T * topk * 20
         q_gbs, r_gbs = q_bytes / (q_ms * 1e-3) / 1e9, r_bytes / (r_ms * 1e-3) / 1e9
+        # the layer's prologue as it runs for this batch: routing, then the global amax and
+        # the quantisation written straight into every slot of each token
+        a_fp4 = torch.empty(cap, K // 2, dtype=torch.uint8, device="cuda")
+        a_sf = torch.empty(cap * K // 16, dtype=torch.uint8, device="cuda")
+
+        def stage_route(i):
+            B.moe_route(ids, w, E, wl.expert_offset, rbuf["counts"], rbuf["offsets"], rbuf["padded_offsets"],
+                        rbuf["slot_token"], rbuf["slot_weight"], rbuf["pair_slot"], rws)
+            B.moe_stage_activation_to_slots(xs[i % nbuf], rbuf["pair_slot"], topk, a_fp4, a_sf, gs, ws=sws)
+
+        f_ms, _ = timed(stage_route)
+        f_bytes = r_bytes + xbytes * (2 if xbytes > L2_BYTES else 1) + T * topk * (K // 2 + K // 16)
+        f_gbs = f_bytes / (f_ms * 1e-3) / 1e9
         out[name] = {
             "workload": f"{wl.name}: T={T}, K={K}, E={E}, top-{topk} (stage_activation and routing alone)",
             "timing": f"device time per call: {reps} calls in one CUDA graph, replayed; us_eager = issued "
@@ -764,8 +851,14 @@ def sweep_configs(pk, B, reps=20):
             "route": {"us": r_ms * 1e3, "us_eager": r_eager * 1e3, "algorithmic_bytes": r_bytes,
                       "roofline": {"bound": "hbm", "achieved": r_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                                    "frac": r_gbs / pk["hbm_gbs"], "peak_source": pk["source"]}},
+            "fused_stage_route": {"us": f_ms * 1e3, "algorithmic_bytes": f_bytes,
+                                  "what": "moe_route then moe_stage_activation_to_slots (amax pass, then each "
+                                          "token quantised once and written to each of its top-k slots)",
+                                  "roofline": {"bound": "hbm", "achieved": f_gbs, "peak": pk["hbm_gbs"],
+                                               "unit": "GB/s", "frac": f_gbs / pk["hbm_gbs"],
+                                               "peak_source": pk["source"]}},
         }
-        del xs, x0, codes, sf, rbuf, rws
+        del xs, x0, codes, sf, rbuf, rws, a_fp4, a_sf
         torch.cuda.empty_cache()
     return out
 
@@ -781,7 +874,7 @@ def run_reference(args, ws, rank):
     wl = workloads.WORKLOADS[args.workload]
     x = workloads.activations(wl)
     ids, w = workloads.routing(wl)
-    n = 2
+    n = 2 if wl.n_global else 1    # a token with all top-k experts local costs the oracle ~1 s per expert
     xs, ids_s, w_s = x[:n].float().numpy(), ids[:n], w[:n]
     E, I, K = wl.E, wl.I, wl.K
     W = {"w1_codes": np.zeros((E, 2 * I, K // 2), np.uint8), "w1_sf": np.zeros((E, 2 * I, K // 16), np.uint8),

@@ -21,11 +21,11 @@
  *    noted (BF16 tensors: 16 bytes).
  *  - Work is enqueued on the caller's stream, never synchronises the host, and
  *    can be captured into a CUDA graph (no host reads of device data).
- *  - Devices: the library looks up launch settings (the SM count, the kernels'
- *    shared-memory limits, the CTA-pair kernel's grid) on its first launch in the
- *    process and reuses them, so a process drives one device (one process per GPU,
- *    the current device at the first call).  Make the first call of each entry point
- *    outside stream capture.
+ *  - Devices: every call runs on the current device.  Launch settings (the SM
+ *    count, the kernels' shared-memory opt-ins, the CTA-pair kernel's grid) are
+ *    looked up on the first call on each device and kept per device (thread-safe),
+ *    so one process may drive several devices, from several host threads.  Make the
+ *    first call of each entry point on a device outside stream capture.
  *  - Return value: MOE_OK, or an error found on the host before anything was
  *    enqueued (MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE),
  *    or MOE_ERR_CUDA if a launch failed.
@@ -229,7 +229,9 @@ moe_status moe_route(const int32_t* topk_ids, const float* topk_w, int64_t T, in
  *   without enqueuing anything.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before capturing a
- *   stream.
+ *   stream.  The address is kept for the life of the process: a device or primary
+ *   context reset (cudaDeviceReset) after that first call is not supported, since
+ *   the library's module may be reloaded at another address.
  *   Every call shares the one array.  Calls ordered on one stream are safe; calls
  *   that can overlap on the GPU (other streams, other host threads) race on it and
  *   corrupt each other's routing.  Nothing needs clearing between calls: both
@@ -258,7 +260,10 @@ moe_status moe_route_static_scratch(const int32_t* topk_ids, const float* topk_w
  *                         moe_stage_activation) into h_fp4 [capacity, I/2] and
  *                         h_sf (swizzled, capacity*I/16); out_bf16 may be NULL or
  *                         receive h as well.
- *   Rows of padding are never written.  K % 128 == 0, I % 64 == 0, E <= 256. */
+ *   Rows of padding are never written.  K % 128 == 0, I % 64 == 0, E <= 256:
+ *   moe_stage_activation quantises any K % 64 == 0, but the layer's hidden size K is
+ *   also the L2 GEMM's output width, which that GEMM covers in tiles of 128 or 256
+ *   columns, so the layer entry points (L1, L2, moe_forward) take K % 128 == 0. */
 moe_status moe_grouped_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float* gs_a,
                                const int32_t* offsets, const int32_t* padded_offsets,
                                int E, int64_t capacity, int K, int I,
@@ -421,6 +426,16 @@ moe_status moe_selftest_bounded_wait(int32_t* dev_status, int32_t* dev_result, m
  * range past pattern 0xFFFFFFFF; MOE_ERR_CUDA if the launch fails. */
 moe_status moe_selftest_codecs(uint32_t first_pattern, int64_t n, uint8_t* e2m1_codes, uint8_t* e4m3_bytes,
                                moe_stream_t stream);
+
+/* Self-test of the SiLU the L1 epilogues apply (the "complete pipeline" commit of the
+ * tests page: h = SiLU(gate) * up in BF16; SiLU(g) = g / (1 + exp(-g))).  For i < n:
+ *   silu_out[i] = the fp32 value the epilogue computes for gate value g[i] before it
+ *                 multiplies by up and rounds h to BF16 (the fast exp and division
+ *                 intrinsics; a few fp32 ulp from the exact value, see the tests).
+ * g, silu_out: device fp32 arrays of n elements owned by the caller.  Returns
+ * MOE_ERR_INVALID_ARG for n < 0 or NULL arrays with n > 0, MOE_ERR_CUDA if the launch
+ * fails. */
+moe_status moe_selftest_silu(const float* g, int64_t n, float* silu_out, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

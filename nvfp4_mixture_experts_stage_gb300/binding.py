@@ -39,6 +39,7 @@ EXPORTS = (
     "moe_cast_output", "moe_forward", "moe_forward_traced", "moe_route_static_scratch",
     "moe_set_gemm_policy", "moe_combine_rows", "moe_selftest_bounded_wait", "moe_fold_gate_up_scales",
     "moe_quantize_weights_workspace_size", "moe_quantize_weights", "moe_selftest_codecs",
+    "moe_selftest_silu",
 )
 
 MOE_GEMM_AUTO, MOE_GEMM_TILED, MOE_GEMM_STREAMING = 0, 1, 2
@@ -85,6 +86,7 @@ def _load():
         "moe_combine_rows": (I32, [P, I64, P, P, I64, I32, I32, I64, P, P, P]),
         "moe_selftest_bounded_wait": (I32, [P, P, P]),
         "moe_selftest_codecs": (I32, [ctypes.c_uint32, I64, P, P, P]),
+        "moe_selftest_silu": (I32, [P, I64, P, P]),
         "moe_fold_gate_up_scales": (I32, [P, P, P, P, I32, I32, I32, P]),
         "moe_quantize_weights_workspace_size": (ctypes.c_size_t, [I32, I32, I32]),
         "moe_quantize_weights": (I32, [P, P, I32, I32, I32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
@@ -266,6 +268,14 @@ def moe_selftest_codecs(first_pattern, e2m1_codes, e4m3_bytes, stream=None):
     assert e4m3_bytes.numel() == n
     _check("moe_selftest_codecs", _lib.moe_selftest_codecs(first_pattern, n, _p(e2m1_codes), _p(e4m3_bytes),
                                                            _stream(stream)))
+
+
+def moe_selftest_silu(g, silu_out, stream=None):
+    """SiLU self-test (see include/moe_stage.h): silu_out[i] = the L1 epilogue's fp32
+    SiLU of g[i] (both fp32 device tensors of the same size)."""
+    n = g.numel()
+    assert silu_out.numel() == n and g.dtype == torch.float32 and silu_out.dtype == torch.float32
+    _check("moe_selftest_silu", _lib.moe_selftest_silu(_p(g), n, _p(silu_out), _stream(stream)))
 
 
 def moe_combine_rows(y_rows, pair_slot, topk_w, out_bf16, capacity=None, dev_status=None, stream=None):

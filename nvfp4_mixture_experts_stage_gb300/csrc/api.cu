@@ -14,16 +14,7 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
+int sm_count() { return sm_count_of_current_device(); }
 
 int64_t route_chunks(int64_t T, int topk) { return ceil_div(T * topk, kRouteChunk); }
 
@@ -203,6 +194,11 @@ moe_status moe_selftest_codecs(uint32_t first_pattern, int64_t n, uint8_t* e2m1_
   if (n < 0 || (n > 0 && (!e2m1_codes || !e4m3_bytes))) return MOE_ERR_INVALID_ARG;
   if ((uint64_t)first_pattern + (uint64_t)n > (1ull << 32)) return MOE_ERR_INVALID_ARG;
   return selftest_codecs(first_pattern, n, e2m1_codes, e4m3_bytes, (cudaStream_t)stream);
+}
+
+moe_status moe_selftest_silu(const float* g, int64_t n, float* silu_out, moe_stream_t stream) {
+  if (n < 0 || (n > 0 && (!g || !silu_out))) return MOE_ERR_INVALID_ARG;
+  return selftest_silu(g, n, silu_out, (cudaStream_t)stream);
 }
 
 int moe_set_gemm_policy(int policy) {

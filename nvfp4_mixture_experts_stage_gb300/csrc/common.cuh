@@ -1,6 +1,7 @@
 // Shared device helpers of the NVFP4 MoE stage (sm_103a).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <utility>
 #include <cuda_runtime.h>
@@ -39,6 +40,61 @@ inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---- per-device launch settings (host) -----------------------------------------
+// Launch settings that depend on the device (SM count, a kernel's shared-memory
+// opt-in, a cluster kernel's grid) are looked up once per device and cached in
+// per-device slots, so one process may drive several devices from several threads.
+// Concurrent first calls on a device may both compute a value; the computations are
+// idempotent and the slot is written atomically.
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices ? d : -1;
+}
+
+// A positive int per device (0 = not yet known).
+struct PerDeviceInt {
+  std::atomic<int> v[kMaxDevices] = {};
+  template <class F>
+  int get(F&& compute) {
+    const int d = current_device();
+    if (d < 0) return compute();
+    int x = v[d].load(std::memory_order_acquire);
+    if (x <= 0) {
+      x = compute();
+      if (x > 0) v[d].store(x, std::memory_order_release);
+    }
+    return x;
+  }
+};
+
+// Runs set_up() (a cudaError_t-returning, idempotent call such as
+// cudaFuncSetAttribute) until it first succeeds on each device.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+  template <class F>
+  cudaError_t run(F&& set_up) {
+    const int d = current_device();
+    const uint64_t bit = d >= 0 ? (1ull << d) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = set_up();
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
+
+inline int sm_count_of_current_device() {
+  static PerDeviceInt cache;
+  return cache.get([] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 1;
+    return n;
+  });
 }
 
 // First error wins.

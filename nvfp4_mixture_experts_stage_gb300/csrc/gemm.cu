@@ -279,13 +279,12 @@ template <int KIND, int BN>
 static moe_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st,
                             bool pdl) {
   constexpr size_t kSmemBytes = sizeof(GemmSmem<BN>) + 1024;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    configured = true;
-  }
+  static PerDeviceOnce configured;
+  if (configured.run([] {
+        return cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+      }) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return launch_ex(grouped_gemm_kernel<KIND, BN>, num_sms(), kGemmThreads, kSmemBytes, st, pdl, ta, tb, p) ==
                  cudaSuccess
              ? MOE_OK

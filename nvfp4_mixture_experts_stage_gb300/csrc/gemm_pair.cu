@@ -320,12 +320,12 @@ template <int KIND>
 static moe_status launch_pair_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                                    const CUtensorMap& tsb, const GemmParams& p, cudaStream_t st, bool pdl) {
   constexpr size_t kSmemBytes = sizeof(PairSmem) + 1024;
-  static int grid = 0;
-  if (!grid) {
+  // as many pairs as can be resident at once (pairs sit in one GPC each); 0 on failure
+  static PerDeviceInt grids;
+  const int grid = grids.get([] {
     if (cudaFuncSetAttribute(grouped_gemm_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    // as many pairs as can be resident at once (pairs sit in one GPC each)
+      return 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
     cfg.blockDim = dim3(kGemmThreads);
@@ -333,9 +333,10 @@ static moe_status launch_pair_kind(const CUtensorMap& ta, const CUtensorMap& tb,
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<KIND>, &cfg) != cudaSuccess ||
         clusters < 1)
-      return MOE_ERR_CUDA;
-    grid = 2 * std::min(clusters, num_sms() / 2);
-  }
+      return 0;
+    return 2 * std::min(clusters, num_sms() / 2);
+  });
+  if (grid <= 0) return MOE_ERR_CUDA;
   return launch_ex(grouped_gemm_pair_kernel<KIND>, dim3((unsigned)grid), dim3(kGemmThreads), kSmemBytes, st, pdl, ta,
                    tb, tsa, tsb, p) == cudaSuccess
              ? MOE_OK

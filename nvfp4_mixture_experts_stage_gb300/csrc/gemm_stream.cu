@@ -583,13 +583,12 @@ template <int KIND, int CHUNK>
 static moe_status launch_chunk(const CUtensorMap& tw, const CUtensorMap& tx, const Params& p, cudaStream_t st,
                                bool pdl) {
   constexpr size_t kSmemBytes = sizeof(Smem<CHUNK>) + 1024;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(stream_gemm_kernel<KIND, CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    configured = true;
-  }
+  static PerDeviceOnce configured;
+  if (configured.run([] {
+        return cudaFuncSetAttribute(stream_gemm_kernel<KIND, CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+      }) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return launch_ex(stream_gemm_kernel<KIND, CHUNK>, num_sms(), kThreads, kSmemBytes, st, pdl, tw, tx, p) ==
                  cudaSuccess
              ? MOE_OK

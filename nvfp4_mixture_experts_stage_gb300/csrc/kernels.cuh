@@ -113,6 +113,7 @@ cudaError_t launch_fold_gate_up(uint8_t* sf, const float* gg, const float* gu, f
 // Bounded-wait self-test (selftest.cu).
 moe_status selftest_bounded_wait(int32_t* status, int32_t* result, cudaStream_t st);
 moe_status selftest_codecs(uint32_t first, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t st);
+moe_status selftest_silu(const float* g, int64_t n, float* s, cudaStream_t st);
 
 // Which grouped-GEMM kernel runs (process-wide; moe_set_gemm_policy).
 int gemm_policy();

@@ -341,12 +341,7 @@ cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_
       (reinterpret_cast<uintptr_t>(a.codes) & 15) == 0) {
     // tasks of kRunElems elements; four 256-thread blocks fit per SM
     const int64_t tasks = a.rows * (int64_t)((a.K + kRunElems - 1) / kRunElems);
-    static int sms = 0;
-    if (!sms) {
-      int dev = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
+    const int sms = sm_count_of_current_device();
     const int b = (int)std::min<int64_t>(std::max<int64_t>((tasks + 7) / 8, 1), (int64_t)sms * 4);
     (void)blocks;
     return launch_ex(quantize_slots_kernel, b, 256, 0, st, pdl, a);

@@ -330,13 +330,12 @@ __global__ void __launch_bounds__(1024) forward_prologue_kernel(PrologueArgs a) 
 }
 
 cudaError_t launch_forward_prologue(const PrologueArgs& a, int amax_blocks, cudaStream_t st) {
-  static bool configured = false;
-  const int smem = 32 * kMaxExperts * (int)sizeof(int);
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(forward_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce configured;
+  cudaError_t e = configured.run([] {
+    return cudaFuncSetAttribute(forward_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                32 * kMaxExperts * (int)sizeof(int));
+  });
+  if (e != cudaSuccess) return e;
   forward_prologue_kernel<<<1 + amax_blocks, 1024, 32 * a.E * sizeof(int), st>>>(a);
   return cudaGetLastError();
 }
@@ -349,13 +348,12 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk
   // take longer than the three launches of the chunked path (8192 pairs: 20 us against
   // ~12 us); the layer's fused prologue still routes up to 8192 pairs in its block 0
   if (P <= kSmallRoutePairs / 2) {
-    static bool configured = false;
-    const int smem = 32 * kMaxExperts * (int)sizeof(int);
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    static PerDeviceOnce configured;
+    cudaError_t e = configured.run([] {
+      return cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  32 * kMaxExperts * (int)sizeof(int));
+    });
+    if (e != cudaSuccess) return e;
     route_small_kernel<<<1, 1024, 32 * E * sizeof(int), st>>>(ids, w, (int)P, topk, E, off, counts, offsets,
                                                               padded_offsets, slot_token, slot_weight, pair_slot,
                                                               capacity, status);

@@ -5,7 +5,9 @@
 //     then return through that flag;
 //   * the two code encoders of the quantisers and the requant epilogue (E2M1 of a
 //     scaled value, UE4M3 of a block scale), evaluated on arbitrary fp32 bit patterns
-//     so that a test can sweep every input.
+//     so that a test can sweep every input;
+//   * the SiLU of the L1 epilogues before its product with up and the BF16 rounding of
+//     h, on caller-given gate values (a test sweeps every BF16 gate value).
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -54,6 +56,17 @@ __global__ void selftest_codecs_kernel(uint32_t first, int64_t n, uint8_t* e2m1,
 moe_status selftest_codecs(uint32_t first, int64_t n, uint8_t* e2m1, uint8_t* e4m3, cudaStream_t st) {
   if (n == 0) return MOE_OK;
   selftest_codecs_kernel<<<num_sms() * 8, 256, 0, st>>>(first, n, e2m1, e4m3);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+__global__ void selftest_silu_kernel(const float* g, int64_t n, float* s) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    s[i] = silu_f32(g[i]);
+}
+
+moe_status selftest_silu(const float* g, int64_t n, float* s, cudaStream_t st) {
+  if (n == 0) return MOE_OK;
+  selftest_silu_kernel<<<num_sms() * 4, 256, 0, st>>>(g, n, s);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -234,22 +234,22 @@ MOE_DEV void wait_bar_drain(uint64_t* bar, uint32_t parity) {
 // h = bf16(silu(g) * u) with silu(g) = g / (1 + exp(-g)).  The exponential and the
 // division use the fast hardware approximations (a few ulp of fp32, far below the
 // bf16 rounding of h); the fused L1 epilogue spends most of its time here.
-MOE_DEV float silu_mul(float g, float u) {
-  const float s = __fdividef(g, 1.0f + __expf(-g));
-  return round_bf16(__fmul_rn(s, u));
-}
+MOE_DEV float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+MOE_DEV float silu_mul(float g, float u) { return round_bf16(__fmul_rn(silu_f32(g), u)); }
 
 // host
+// The driver's tensor-map encoder (the same for every device); looked up once, under
+// the thread-safe initialisation of a function-local static.
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+  }();
   return fn;
 }
 
@@ -285,14 +285,6 @@ inline bool make_tmap_plain(CUtensorMap* map, const void* base, uint64_t row_byt
   return r == CUDA_SUCCESS;
 }
 
-inline int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  }
-  return n;
-}
+inline int num_sms() { return sm_count_of_current_device(); }
 
 }  // namespace moe

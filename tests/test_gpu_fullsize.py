@@ -3,9 +3,12 @@
 * decode (T=256, K=4096, I=3072, 48 of 384 experts, top-8): every output
   token against the oracle, with the h scale derived from the data and with
   it held fixed (the calibrated mode bench.py times);
-* prefill (T=8192) and the two skewed workloads: outputs of sampled tokens
-  (including the rows with amax up to 1e4 and tokens of the largest and
-  smallest experts), fixed h scale so the oracle needs only those tokens;
+* prefill (T=8192) and the two skewed workloads: outputs of sampled tokens,
+  chosen so that every 128-row m-tile of every expert's slot range has a row
+  compared element by element (the last row of each m-tile, which includes each
+  expert's last valid row), plus the rows with amax up to 1e4 and tokens of the
+  largest and smallest experts; fixed h scale so the oracle needs only those
+  tokens;
 * quantisation of the full prefill activations and of the 16k x 7168 sweep,
   bit-exact; the 64k x 7168 sweep on sampled rows.
 
@@ -20,6 +23,7 @@ import torch
 
 import workloads
 from oracle import moe as omoe, nvfp4 as q
+from oracle.route import route as oracle_route
 from tests.helpers import assert_layer_close, bf16_dev
 
 pytestmark = pytest.mark.gpu
@@ -108,9 +112,32 @@ def test_decode_every_token_dynamic_and_fixed(layer, decode_ref, policy):
         B.moe_set_gemm_policy(old)
 
 
+def _cover_tokens(wl, ids):
+    """Tokens whose slots include the last row of every 128-row m-tile of every expert
+    (the oracle's slot order), so each tile of both grouped GEMMs has a compared row."""
+    rt = oracle_route(ids, np.ones(ids.shape, np.float32), wl.E, wl.expert_offset)
+    toks, tiles = set(), 0
+    for e in range(wl.E):
+        lo, n = int(rt["padded_offsets"][e]), int(rt["counts"][e])
+        for m0 in range(0, n, 128):
+            toks.add(int(rt["slot_token"][lo + min(m0 + 127, n - 1)]))
+            tiles += 1
+    return np.array(sorted(toks), np.int64), tiles, rt
+
+
 def _sampled(layer, full_weights, wl, tokens):
     gs_h = workloads.fixed_gs_h(wl)
     got, _, x, ids, w = _gpu_forward(layer, wl, B.MOE_GS_FIXED, gs_h=gs_h)
+    ids_np = np.asarray(ids)
+    cover, tiles, rt = _cover_tokens(wl, ids_np)
+    tokens = np.unique(np.concatenate([np.asarray(tokens, np.int64), cover]))
+    # every (expert, m-tile) has at least one slot row among the compared tokens
+    want = np.zeros(wl.T, bool)
+    want[tokens] = True
+    for e in range(wl.E):
+        lo, n = int(rt["padded_offsets"][e]), int(rt["counts"][e])
+        for m0 in range(0, n, 128):
+            assert want[rt["slot_token"][lo + m0:lo + min(m0 + 128, n)]].any(), (e, m0)
     ref = omoe.forward(x.float().numpy(), ids, w, wl.E, wl.expert_offset, full_weights, gs_h=gs_h, tokens=tokens)
     assert_layer_close(got[tokens], ref["out"], wl.name)
     return got, x, ids

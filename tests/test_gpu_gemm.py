@@ -3,7 +3,10 @@
 Exact-arithmetic cases (block scales that are powers of two, alpha = 1, sums
 well inside fp32's 24-bit range) must match bit for bit whatever the
 summation order: they pin the operand and scale layouts and the gate/up
-split.  General cases use the layer tolerance."""
+split, up to the layer's production contraction (K = 4096 for L1, I = 3072 for
+L2).  General cases use the layer tolerance."""
+
+import functools
 
 import numpy as np
 import pytest
@@ -61,16 +64,20 @@ def _rand_operands(r, rows, K, exact):
     if exact:
         # every partial sum is a multiple of the smallest product unit and stays below
         # 2**24 units: K <= 256 with scales 0.25..4 (units 2**-6, |sum| <= 256*36*16),
-        # K <= 1024 with scales 0.5..2 (units 2**-4, |sum| <= 1024*36*4)
+        # K <= 4096 with scales 0.5..2 (units 2**-4, |sum| <= 4096*36*4 = 589824 =
+        # 9437184 units)
         pool = POW2_BYTES if K <= 256 else POW2_BYTES_NARROW
-        assert K <= 1024
+        assert K <= 4096
         sf = pool[r.integers(0, pool.size, (rows, K // 16))]
     else:
         sf = r.integers(0x20, 0x58, (rows, K // 16)).astype(np.uint8)
     return codes, sf
 
 
-def _l1_case(counts, K, I, exact, seed, epilogue, gs=None, tight=False):
+@functools.lru_cache(maxsize=None)
+def _l1_ref(counts, K, I, exact, seed, gs, tight):
+    """Operands and the oracle's g, u for one L1 case (computed once for all five kernel
+    choices)."""
     r = np.random.default_rng(seed)
     rt, cap = _slots(counts, tight=tight)
     E = len(counts)
@@ -84,6 +91,17 @@ def _l1_case(counts, K, I, exact, seed, epilogue, gs=None, tight=False):
         gs_a = np.float32(gs)
         gg = r.uniform(1e-3, 2e-3, E).astype(np.float32)
         gu = r.uniform(1e-3, 2e-3, E).astype(np.float32)
+    g, u = omoe.gemm_l1(a_codes, a_sf, gs_a, rt, w1c, w1s, gg, gu)
+    valid = np.zeros(cap, bool)
+    for e in range(E):
+        valid[rt["padded_offsets"][e]:rt["padded_offsets"][e] + rt["counts"][e]] = True
+    return rt, cap, a_codes, a_sf, w1c, w1s, gs_a, gg, gu, g, u, valid
+
+
+def _l1_case(counts, K, I, exact, seed, epilogue, gs=None, tight=False):
+    rt, cap, a_codes, a_sf, w1c, w1s, gs_a, gg, gu, g, u, valid = _l1_ref(tuple(counts), K, I, exact, seed, gs,
+                                                                           tight)
+    E = len(counts)
     d_wsf = torch.empty(w1s.size, dtype=torch.uint8, device="cuda")
     B.moe_prepare_weights(dev(w1s), d_wsf, E, 2 * I, K, B.MOE_PREP_W1)
     out_cols = 2 * I if epilogue == B.MOE_L1_GATEUP_BF16 else I
@@ -95,15 +113,11 @@ def _l1_case(counts, K, I, exact, seed, epilogue, gs=None, tight=False):
                           out_bf16=out, h_amax=amax, dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
-    g, u = omoe.gemm_l1(a_codes, a_sf, gs_a, rt, w1c, w1s, gg, gu)
-    valid = np.zeros(cap, bool)
-    for e in range(E):
-        valid[rt["padded_offsets"][e]:rt["padded_offsets"][e] + rt["counts"][e]] = True
     return out.float().cpu().numpy(), g, u, valid, amax.item()
 
 
 @pytest.mark.parametrize("counts,K,I", [([5, 0, 140], 256, 128), ([1], 256, 64), ([128, 129, 3, 0, 0, 77], 256, 192),
-                                        ([300, 17], 512, 64)])
+                                        ([300, 17], 512, 64), ([200, 0, 129], 4096, 3072)])
 def test_l1_gateup_exact_arithmetic_bit_exact(counts, K, I):
     got, g, u, valid, _ = _l1_case(counts, K, I, True, 11, B.MOE_L1_GATEUP_BF16)
     assert np.array_equal(got[valid, :I], g[valid])
@@ -137,7 +151,10 @@ def test_l1_silu_and_amax():
     assert amax == np.abs(got[valid]).max()
 
 
-def _l2_case(counts, I, K, exact, seed, epilogue, gs=None, slot_token=None, slot_weight=None, T=0, tight=False):
+@functools.lru_cache(maxsize=None)
+def _l2_ref(counts, I, K, exact, seed, gs, tight):
+    """Operands and the oracle's y for one L2 case (computed once for all five kernel
+    choices)."""
     r = np.random.default_rng(seed)
     rt, cap = _slots(counts, tight=tight)
     E = len(counts)
@@ -147,6 +164,16 @@ def _l2_case(counts, I, K, exact, seed, epilogue, gs=None, slot_token=None, slot
     w2s = w2s.reshape(E, K, I // 16)
     gs_h = np.float32(1 if gs is None else gs)
     g2 = np.ones(E, np.float32) if gs is None else r.uniform(1e-3, 2e-3, E).astype(np.float32)
+    ref = omoe.gemm_l2(h_codes, h_sf, gs_h, rt, w2c, w2s, g2)
+    valid = np.zeros(cap, bool)
+    for e in range(E):
+        valid[rt["padded_offsets"][e]:rt["padded_offsets"][e] + rt["counts"][e]] = True
+    return rt, cap, h_codes, h_sf, w2c, w2s, gs_h, g2, ref, valid
+
+
+def _l2_case(counts, I, K, exact, seed, epilogue, gs=None, slot_token=None, slot_weight=None, T=0, tight=False):
+    rt, cap, h_codes, h_sf, w2c, w2s, gs_h, g2, ref, valid = _l2_ref(tuple(counts), I, K, exact, seed, gs, tight)
+    E = len(counts)
     d_wsf = torch.empty(w2s.size, dtype=torch.uint8, device="cuda")
     B.moe_prepare_weights(dev(w2s), d_wsf, E, K, I, B.MOE_PREP_W2)
     y = torch.zeros(cap, K, dtype=torch.bfloat16, device="cuda")
@@ -159,15 +186,11 @@ def _l2_case(counts, I, K, exact, seed, epilogue, gs=None, slot_token=None, slot
                           dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
-    ref = omoe.gemm_l2(h_codes, h_sf, gs_h, rt, w2c, w2s, g2)
-    valid = np.zeros(cap, bool)
-    for e in range(E):
-        valid[rt["padded_offsets"][e]:rt["padded_offsets"][e] + rt["counts"][e]] = True
     return y.float().cpu().numpy(), ref, valid, out32.cpu().numpy(), rt
 
 
 @pytest.mark.parametrize("counts,I,K", [([5, 0, 140], 128, 256), ([128, 3], 256, 384), ([1, 1, 1], 64, 128),
-                                        ([260], 512, 128)])
+                                        ([260], 512, 128), ([200, 0, 129], 3072, 4096)])
 def test_l2_rows_exact_arithmetic_bit_exact(counts, I, K):
     got, ref, valid, _, _ = _l2_case(counts, I, K, True, 21, B.MOE_L2_ROWS_BF16)
     assert np.array_equal(got[valid], ref[valid])

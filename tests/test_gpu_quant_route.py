@@ -71,6 +71,30 @@ def test_stage_activation_fixed_scale_bit_exact(gs_fixed):
     assert np.array_equal(sf.reshape(48, 16), rs)
 
 
+def _golden_blocks():
+    from tests.test_oracle_quantize import _golden_blocks as g
+    return g()
+
+
+@pytest.mark.parametrize("case", _golden_blocks(), ids=lambda c: c[0])
+def test_hand_derived_blocks_on_device(case):
+    """The hand-derived blocks of tests/golden/quant_blocks.txt (derived from the pages'
+    encoding, not from either implementation) through the device quantiser: the block
+    sits first in a 64-wide row of zeros (the API quantises 64 columns at a time), so its
+    scale byte and codes must be the golden ones; "data" cases take the global scale from
+    the row's amax (the block's own).  Every input is a BF16 value, subnormals included."""
+    name, gs, x, sb, nibs, bts = case
+    row = np.zeros((1, 64), np.float32)
+    row[0, :16] = x
+    assert np.array_equal(q.bf16_round(row), row)          # BF16 inputs, exactly
+    codes, sf, g = _stage(row, 0, gs)
+    assert sf[0] == sb
+    assert list(codes[0, :8]) == bts
+    assert not codes[0, 8:].any() and not sf[1:4].any()
+    if gs is None:
+        assert g == np.float32(1.0)
+
+
 def _finite_bf16():
     f = q.bf16_from_bits(np.arange(65536, dtype=np.uint32).astype(np.uint16))
     return f[np.isfinite(f)]

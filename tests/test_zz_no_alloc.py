@@ -65,6 +65,25 @@ def test_static_scratch_route_matches_moe_route_twice_in_a_row(B):
               _with_workspace(B, ids_d, w_d, wl.E, wl.expert_offset))
 
 
+def test_static_scratch_two_table_calls_in_a_row(B):
+    """Two calls in a row that both use the fixed tables (above 4096 (token, k) pairs
+    routing goes through the chunk tables; below, one block routes without them), with
+    different routings and expert counts, so the second call runs over the first call's
+    table contents."""
+    skew = workloads.WORKLOADS["skew_top8"]             # 32768 pairs, 48 experts
+    ids1, w1 = workloads.routing(skew)
+    r = np.random.default_rng(11)
+    ids2 = r.integers(-3, 110, (2000, 8)).astype(np.int32)   # 16000 pairs, 100 experts at offset 5
+    w2 = r.random((2000, 8)).astype(np.float32)
+    assert ids1.size > 4096 and ids2.size > 4096
+    d = lambda a: torch.from_numpy(a).cuda()
+    o1 = _without_workspace(B, d(ids1), d(w1), skew.E, 0)
+    torch.cuda.synchronize()
+    o2 = _without_workspace(B, d(ids2), d(w2), 100, 5)
+    _same(o1, _with_workspace(B, d(ids1), d(w1), skew.E, 0))
+    _same(o2, _with_workspace(B, d(ids2), d(w2), 100, 5))
+
+
 def test_static_scratch_route_back_to_back_on_one_stream(B):
     # a large call then a small one, enqueued without a host sync in between
     big = workloads.WORKLOADS["prefill"]
