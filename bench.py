@@ -835,7 +835,7 @@ def sweep_configs(pk, B, reps=20):
         def stage_route(i):
             B.moe_route(ids, w, E, wl.expert_offset, rbuf["counts"], rbuf["offsets"], rbuf["padded_offsets"],
                         rbuf["slot_token"], rbuf["slot_weight"], rbuf["pair_slot"], rws)
-            B.moe_stage_activation_to_slots(xs[i % nbuf], rbuf["pair_slot"], topk, a_fp4, a_sf, gs, ws=sws)
+            B.moe_stage_activation_to_slots(xs[i % nbuf], rbuf["pair_slot"], topk, cap, a_fp4, a_sf, gs, ws=sws)
 
         f_ms, _ = timed(stage_route)
         f_bytes = r_bytes + xbytes * (2 if xbytes > L2_BYTES else 1) + T * topk * (K // 2 + K // 16)
