@@ -13,7 +13,7 @@
 // 128-row blocks, each 64 gate rows then the matching 64 up rows (128 h columns).
 // One CTA per SM, 12 warps:
 //   warp 0      TMA producer: A (slot rows), B (weight rows) and their scale atoms
-//               into a shared-memory ring (full/empty mbarriers).
+//               into a shared-memory ring (full/empty mbarriers), four loads per stage.
 //   warp 1      MMA issuer and TMEM owner: only tcgen05.mma (M=128, N=BN, K=64),
 //               four per stage, into one TMEM accumulator of BN columns.
 //   warps 2, 3  scale copiers: once a stage's scale atoms have landed, tcgen05.cp of
@@ -74,7 +74,7 @@ struct __align__(1024) GemmSmem {
 template <int KIND, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmap_sfb, const GemmParams p) {
   using C = TiledCfg<BN>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -136,30 +136,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row_a = s.poff[e] + m * kBM;
         const uint8_t* sfa_src = p.a_sf + ((int64_t)(row_a >> 7) * ksf4) * 512;
         // prepared weight row blocks n*kBlocks .. n*kBlocks + kBlocks - 1 of expert e
-        const uint8_t* sfb_src =
-            p.b_sf + ((int64_t)e * (p.b_rows >> 7) + (int64_t)n * C::kBlocks) * (int64_t)ksf4 * 512;
+        const int sfb_block = e * (p.b_rows >> 7) + n * C::kBlocks;
+        // four loads per stage (the producer's issue time, not the bytes, bounds how fast
+        // stages arrive): A rows; the tile's weight rows in one box (L1: kBlocks blocks of
+        // 64 gate then 64 up rows, a 5-D box); the A scale atoms; the weight scale atoms of
+        // all kBlocks blocks in one 3-D box (a short last stage reads zeros past the row end)
         for (int kb = 0; kb < nkb; ++kb) {
           const int natoms = min(4, ksf4 - 4 * kb);
           if (!wait_bar_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.full[stage], C::kAStage + C::kBStage);
-          mbar_arrive_expect_tx(&s.sf_full[stage], (1 + C::kBlocks) * natoms * 512);
+          mbar_arrive_expect_tx(&s.sf_full[stage], natoms * 512 + C::kSfbStage);
           const int x = kb * kBKBytes;
           tma_load_2d(s.a[stage], &tmap_a, &s.full[stage], x, row_a);
-#pragma unroll
-          for (int j = 0; j < C::kBlocks; ++j) {  // weight block j (128 rows)
-            uint8_t* dst = s.b[stage] + j * 128 * kBKBytes;
-            if (kL1) {
-              // 64 gate rows then the matching 64 up rows (h columns n*BN/2 + 64 j ..)
-              const int yb = e * p.b_rows + n * (BN / 2) + 64 * j;
-              tma_load_2d(dst, &tmap_b, &s.full[stage], x, yb);
-              tma_load_2d(dst + 64 * kBKBytes, &tmap_b, &s.full[stage], x, yb + p.I);
-            } else {
-              tma_load_2d(dst, &tmap_b, &s.full[stage], x, e * p.b_rows + n * BN + 128 * j);
-            }
-            bulk_load(s.sfb[stage] + j * 4 * 512, sfb_src + (int64_t)j * ksf4 * 512 + kb * 4 * 512, natoms * 512,
-                      &s.sf_full[stage]);
-          }
+          if (kL1)
+            tma_load_5d(s.b[stage], &tmap_b, &s.full[stage], x, 0, 0, n * C::kBlocks, e);
+          else
+            tma_load_2d(s.b[stage], &tmap_b, &s.full[stage], x, e * p.b_rows + n * BN);
           bulk_load(s.sfa[stage], sfa_src + kb * 4 * 512, natoms * 512, &s.sf_full[stage]);
+          tma_load_3d(s.sfb[stage], &tmap_sfb, &s.sf_full[stage], 0, 8 * kb, sfb_block);
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -276,8 +270,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <int KIND, int BN>
-static moe_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st,
-                            bool pdl) {
+static moe_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsb, const GemmParams& p,
+                            cudaStream_t st, bool pdl) {
   constexpr size_t kSmemBytes = sizeof(GemmSmem<BN>) + 1024;
   static PerDeviceOnce configured;
   if (configured.run([] {
@@ -285,16 +279,18 @@ static moe_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const 
                                     (int)kSmemBytes);
       }) != cudaSuccess)
     return MOE_ERR_CUDA;
-  return launch_ex(grouped_gemm_kernel<KIND, BN>, num_sms(), kGemmThreads, kSmemBytes, st, pdl, ta, tb, p) ==
+  return launch_ex(grouped_gemm_kernel<KIND, BN>, num_sms(), kGemmThreads, kSmemBytes, st, pdl, ta, tb, tsb, p) ==
                  cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
 
+// ta: slot rows (boxes of 128 rows); tb: weight rows (L1: make_tmap_w1_blocks with bn/128
+// blocks per box; L2: boxes of bn rows); tsb: the prepared weight scales (bn/128 blocks).
 template <int KIND>
-static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int bn,
-                              cudaStream_t st, bool pdl) {
-  return bn == 256 ? launch_bn<KIND, 256>(ta, tb, p, st, pdl) : launch_bn<KIND, 128>(ta, tb, p, st, pdl);
+static moe_status launch_kind(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsb,
+                              const GemmParams& p, int bn, cudaStream_t st, bool pdl) {
+  return bn == 256 ? launch_bn<KIND, 256>(ta, tb, tsb, p, st, pdl) : launch_bn<KIND, 128>(ta, tb, tsb, p, st, pdl);
 }
 
 static int g_policy = MOE_GEMM_AUTO;
@@ -335,10 +331,9 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
   if (use_stream_gemm(cap, E, K))
     return launch_stream_gemm_l1(a_fp4, a_sf, gs_a, offsets, padded_offsets, E, cap, K, I, w1_fp4, w1_sf, gs_g, gs_u,
                                  epilogue, out_bf16, h_amax, h_fp4, h_sf, gs_h, status, st, pdl);
-  CUtensorMap ta, tb;
-  if (!make_tmap(&ta, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
-  if (!make_tmap(&tb, w1_fp4, (uint64_t)K / 2, (uint64_t)E * 2 * I, 64)) return MOE_ERR_CUDA;
   const int bn = I % 128 == 0 ? 256 : 128;
+  CUtensorMap ta, tb, tsb;
+  if (!make_tmap(&ta, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
   GemmParams p{};
   p.a_sf = a_sf;
   p.b_sf = w1_sf;
@@ -368,12 +363,17 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
     const int kind = epilogue == MOE_L1_GATEUP_BF16 ? kL1GateUp : epilogue == MOE_L1_SILU_BF16 ? kL1Silu : kL1Requant;
     if (epilogue != MOE_L1_GATEUP_BF16 && epilogue != MOE_L1_SILU_BF16 && epilogue != MOE_L1_SILU_REQUANT)
       return MOE_ERR_INVALID_ARG;
+    // each CTA of a pair loads one 64 gate + 64 up row block
+    if (!make_tmap_w1_blocks(&tb, w1_fp4, (uint64_t)K / 2, I, E, 1)) return MOE_ERR_CUDA;
     return launch_pair_gemm(kind, ta, tb, p, st, pdl);
   }
+  if (!make_tmap_w1_blocks(&tb, w1_fp4, (uint64_t)K / 2, I, E, bn / 128) ||
+      !make_tmap_sf_blocks(&tsb, w1_sf, K / 64, (uint64_t)E * (2 * I / 128), bn / 128))
+    return MOE_ERR_CUDA;
   switch (epilogue) {
-    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, p, bn, st, pdl);
-    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, p, bn, st, pdl);
-    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(ta, tb, p, bn, st, pdl);
+    case MOE_L1_GATEUP_BF16: return launch_kind<kL1GateUp>(ta, tb, tsb, p, bn, st, pdl);
+    case MOE_L1_SILU_BF16: return launch_kind<kL1Silu>(ta, tb, tsb, p, bn, st, pdl);
+    case MOE_L1_SILU_REQUANT: return launch_kind<kL1Requant>(ta, tb, tsb, p, bn, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }
@@ -387,10 +387,12 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
   if (use_stream_gemm(cap, E, I))
     return launch_stream_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, cap, I, K, w2_fp4, w2_sf, gs_w2,
                                  epilogue, y_rows, slot_token, slot_weight, out32, T, status, st, pdl);
-  CUtensorMap ta, tb;
-  if (!make_tmap(&ta, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
-  if (!make_tmap(&tb, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, 128)) return MOE_ERR_CUDA;
   const int bn = K % 256 == 0 ? 256 : 128;
+  const bool pair = bn == 256 && pair_gemm_enabled(false);
+  CUtensorMap ta, tb, tsb;
+  if (!make_tmap(&ta, h_fp4, (uint64_t)I / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
+  // boxes of one tile's weight rows (a CTA pair: each CTA 128 of them)
+  if (!make_tmap(&tb, w2_fp4, (uint64_t)I / 2, (uint64_t)E * K, pair ? 128 : bn)) return MOE_ERR_CUDA;
   GemmParams p{};
   p.a_sf = h_sf;
   p.b_sf = w2_sf;
@@ -412,13 +414,14 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
   p.out_cols = K;
   p.cap = cap;
   p.status = status;
-  if (bn == 256 && pair_gemm_enabled(false)) {
+  if (pair) {
     if (epilogue != MOE_L2_ROWS_BF16 && epilogue != MOE_L2_SCATTER) return MOE_ERR_INVALID_ARG;
     return launch_pair_gemm(epilogue == MOE_L2_ROWS_BF16 ? kL2Rows : kL2Scatter, ta, tb, p, st, pdl);
   }
+  if (!make_tmap_sf_blocks(&tsb, w2_sf, I / 64, (uint64_t)E * (K / 128), bn / 128)) return MOE_ERR_CUDA;
   switch (epilogue) {
-    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, p, bn, st, pdl);
-    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, p, bn, st, pdl);
+    case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(ta, tb, tsb, p, bn, st, pdl);
+    case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(ta, tb, tsb, p, bn, st, pdl);
   }
   return MOE_ERR_INVALID_ARG;
 }

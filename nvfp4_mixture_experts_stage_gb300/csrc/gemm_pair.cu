@@ -164,9 +164,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const bool has_rows = m < mt;
         const bool peer_rows = 2 * mp + 1 < mt;
         const int row_a = s.poff[e] + m * kBM;
-        // scale atoms as rows of 256 B: a stage's four atoms are eight rows
+        // scale atoms as rows of 256 B: a stage's four atoms are eight rows; the weight
+        // scales of prepared blocks 2n and 2n + 1 come in one 3-D box
         const int sfa_row = ((row_a >> 7) * ksf4) * 2;
-        const int sfb_row = ((e * (p.b_rows >> 7) + n * 2) * ksf4) * 2;  // prepared block 2n; 2n + 1 follows
+        const int sfb_block = e * (p.b_rows >> 7) + n * 2;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bar_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (rank == 0) {
@@ -180,15 +181,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                          fb = full0 + 8 * stage;
           const int x = kb * kBKBytes;
           if (has_rows) tma_load_2d_pair(s.sfa[stage], &tmap_sfa, sfb, 0, sfa_row + 8 * kb);
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_load_2d_pair(s.sfb[stage] + j * 4 * 512, &tmap_sfb, sfb, 0, sfb_row + j * 2 * ksf4 + 8 * kb);
+          tma_load_3d_pair(s.sfb[stage], &tmap_sfb, sfb, 0, 8 * kb, sfb_block);
           if (has_rows) tma_load_2d_pair(s.a[stage], &tmap_a, fb, x, row_a);
           if (kL1) {
-            // prepared block 2n + rank: 64 gate rows then the matching 64 up rows
-            const int yb = e * p.b_rows + n * 128 + 64 * (int)rank;
-            tma_load_2d_pair(s.b[stage], &tmap_b, fb, x, yb);
-            tma_load_2d_pair(s.b[stage] + 64 * kBKBytes, &tmap_b, fb, x, yb + p.I);
+            // prepared block 2n + rank: 64 gate rows then the matching 64 up rows (one 5-D box)
+            tma_load_5d_pair(s.b[stage], &tmap_b, fb, x, 0, 0, 2 * n + (int)rank, e);
           } else {
             tma_load_2d_pair(s.b[stage], &tmap_b, fb, x, e * p.b_rows + n * 256 + 128 * (int)rank);
           }
@@ -349,8 +346,8 @@ moe_status launch_pair_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& 
   // reads the following atoms, or zeros past the end, which no MMA uses)
   CUtensorMap tsa, tsb;
   const uint64_t sfa_rows = (uint64_t)p.cap * (uint64_t)p.Kred / 16 / 256;
-  const uint64_t sfb_rows = (uint64_t)p.E * (uint64_t)p.b_rows * (uint64_t)p.Kred / 16 / 256;
-  if (!make_tmap_plain(&tsa, p.a_sf, 256, sfa_rows, 8) || !make_tmap_plain(&tsb, p.b_sf, 256, sfb_rows, 8))
+  if (!make_tmap_plain(&tsa, p.a_sf, 256, sfa_rows, 8) ||
+      !make_tmap_sf_blocks(&tsb, p.b_sf, p.Kred / 64, (uint64_t)p.E * (uint64_t)(p.b_rows / 128), 2))
     return MOE_ERR_CUDA;
   switch (kind) {
     case kL1GateUp: return launch_pair_kind<kL1GateUp>(ta, tb, tsa, tsb, p, st, pdl);

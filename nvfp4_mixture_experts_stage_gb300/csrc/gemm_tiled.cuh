@@ -269,7 +269,8 @@ MOE_DEV void epilogue_finish(const GemmParams& p, float amax) {
 }
 
 // The CTA-pair kernel (host): ta = slot rows [cap, Kred/2] in boxes of 128 rows, tb =
-// weight rows in boxes of 64 (L1) or 128 (L2) rows, kind a GemmKind.
+// weight rows (L1: make_tmap_w1_blocks with one block per box; L2: boxes of 128 rows),
+// kind a GemmKind.
 moe_status launch_pair_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                             cudaStream_t st, bool pdl);
 bool pair_gemm_enabled(bool l1);

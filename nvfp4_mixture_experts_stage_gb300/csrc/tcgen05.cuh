@@ -49,6 +49,37 @@ MOE_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, i
       "l"(map), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
+// 3-D and 5-D tiled loads (one instruction for a box the 2-D map would need several
+// of: the gate and up halves of a W1 row block, the scale atoms of two weight blocks).
+MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+MOE_DEV void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+MOE_DEV void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+MOE_DEV void tma_load_5d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2, int c3,
+                              int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
 MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -280,6 +311,40 @@ inline bool make_tmap_plain(CUtensorMap* map, const void* base, uint64_t row_byt
   cuuint32_t box[2] = {(cuuint32_t)row_bytes, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// W1 codes [E, 2I, row_bytes] (gate rows 0..I-1, up rows I..2I-1 of each expert) seen as
+// 5-D (byte, row in a 64-row block, half: gate/up, block, expert), 128-byte swizzle; one
+// box = `blocks` consecutive 64-row blocks, each as 64 gate rows then the matching 64 up
+// rows (the L1 tile's layout), 128 bytes of contraction.
+inline bool make_tmap_w1_blocks(CUtensorMap* map, const void* base, uint64_t row_bytes, int I, int E, int blocks) {
+  auto enc = tensor_map_encoder();
+  if (!enc || I % 64) return false;
+  cuuint64_t dims[5] = {row_bytes, 64, 2, (cuuint64_t)(I / 64), (cuuint64_t)E};
+  cuuint64_t strides[4] = {row_bytes, (cuuint64_t)I * row_bytes, 64 * row_bytes, 2ull * I * row_bytes};
+  cuuint32_t box[5] = {128u, 64u, 2u, (cuuint32_t)blocks, 1u};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Prepared weight scales (E * blocks_per_expert blocks of 128 rows, each k_sf4 atoms of
+// 512 bytes) seen as 3-D (byte in a 256-byte row, row in a block: 2 per atom, block);
+// one box = one stage's four atoms (8 rows) of `blocks` consecutive blocks.  Rows past a
+// block's end (a last stage with fewer than four atoms) read as zeros.
+inline bool make_tmap_sf_blocks(CUtensorMap* map, const void* base, int k_sf4, uint64_t nblocks, int blocks) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {256, (cuuint64_t)(2 * k_sf4), nblocks};
+  cuuint64_t strides[2] = {256, (cuuint64_t)k_sf4 * 512};
+  cuuint32_t box[3] = {256u, 8u, (cuuint32_t)blocks};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
