@@ -7,17 +7,23 @@
 // device, zero-weight padding) and of tests ("token layout": rows grouped
 // [expert 0 | expert 1 | ...]).
 //
-// Three launches over chunks of 256 (token, k) pairs, one chunk per warp:
-//   count: warp-level histogram (__match_any_sync groups equal experts, the
-//          group leader adds the group size) -> cnt[e][chunk];
-//   scan:  one block; per expert a warp-level prefix sum over chunks gives each
-//          chunk's first rank, then a scan over experts gives offsets and
-//          128-padded offsets;
-//   place: each warp walks its chunk again in order, ranks pairs within the
-//          32-pair group by popcount of the lower lanes of its match group, and
-//          writes slot_token / slot_weight / pair_slot.
-// Processing every chunk in order and every group in lane order makes the
-// placement stable: slots of an expert follow ascending t*topk + j.
+// Large batches: one cooperative launch over chunks of 256 (token, k) pairs, one chunk
+// per warp at a time, in three phases separated by grid-wide barriers:
+//   count: warp-level histogram (__match_any_sync groups equal experts, the group
+//          leader adds the group size) -> cnt[e][chunk];
+//   scan:  per expert a warp-level prefix sum over chunks gives each chunk's first
+//          rank; every block then scans the expert totals into offsets and 128-padded
+//          offsets;
+//   place: each warp walks its chunks again in order, ranks pairs within the 32-pair
+//          group by popcount of the lower lanes of its match group, and writes
+//          slot_token / slot_weight / pair_slot; the blocks fill the padding slots.
+// Processing every chunk in order and every group in lane order makes the placement
+// stable: slots of an expert follow ascending t*topk + j.  Small batches route in one
+// block (route_small_kernel).
+#include <algorithm>
+
+#include <cooperative_groups.h>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -28,38 +34,52 @@ __device__ __forceinline__ int local_expert(const int32_t* ids, int64_t idx, int
   return (l >= 0 && l < E) ? l : -1;
 }
 
-__global__ void __launch_bounds__(kRouteWarps * 32) route_count_kernel(
-    const int32_t* __restrict__ ids, int64_t P, int E, int off, int32_t* __restrict__ cnt, int nchunks) {
-  __shared__ int hist[kRouteWarps][kMaxExperts];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int chunk = blockIdx.x * kRouteWarps + warp;
-  if (chunk >= nchunks) return;  // whole warp leaves together
-  for (int e = lane; e < E; e += 32) hist[warp][e] = 0;
-  __syncwarp();
-  const int64_t base = (int64_t)chunk * kRouteChunk;
+namespace cg = cooperative_groups;
+
+// Per-warp histogram of one chunk's local experts into hist[0..E) (shared memory).
+__device__ __forceinline__ void chunk_histogram(const int32_t* __restrict__ ids, int64_t base, int64_t P, int off,
+                                                int E, int* hist) {
+  const int lane = threadIdx.x & 31;
   int loc[kRouteChunk / 32];
 #pragma unroll
   for (int g = 0; g < kRouteChunk / 32; ++g) loc[g] = local_expert(ids, base + g * 32 + lane, P, off, E);
 #pragma unroll
   for (int g = 0; g < kRouteChunk / 32; ++g) {
     const unsigned grp = __match_any_sync(0xFFFFFFFFu, loc[g]);
-    if (loc[g] >= 0 && lane == __ffs(grp) - 1) hist[warp][loc[g]] += __popc(grp);
+    if (loc[g] >= 0 && lane == __ffs(grp) - 1) hist[loc[g]] += __popc(grp);
     __syncwarp();
   }
-  for (int e = lane; e < E; e += 32) cnt[(int64_t)e * nchunks + chunk] = hist[warp][e];
 }
 
-// One block of 1024 threads.
-__global__ void __launch_bounds__(1024) route_scan_kernel(
-    const int32_t* __restrict__ cnt, int nchunks, int E, int32_t* __restrict__ base,
-    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets) {
-  __shared__ int s_cnt[kMaxExperts];
+// Launched cooperatively with blockDim kRouteWarps * 32 and a grid that fits on the GPU
+// at once.  cnt, base: E * nchunks ints of scratch.
+__global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t P, int topk, int E, int off,
+    int32_t* __restrict__ cnt, int32_t* __restrict__ base, int nchunks, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets, int32_t* __restrict__ slot_token,
+    float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot, int64_t capacity, int32_t* status) {
+  __shared__ int run[kRouteWarps][kMaxExperts];
+  __shared__ int s_cnt[kMaxExperts], s_poff[kMaxExperts + 1];
+  cg::grid_group grid = cg::this_grid();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += 32) {
+  const int gw = blockIdx.x * kRouteWarps + warp, nw = gridDim.x * kRouteWarps;
+
+  // count
+  for (int chunk = gw; chunk < nchunks; chunk += nw) {
+    for (int e = lane; e < E; e += 32) run[warp][e] = 0;
+    __syncwarp();
+    chunk_histogram(ids, (int64_t)chunk * kRouteChunk, P, off, E, run[warp]);
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) cnt[(int64_t)e * nchunks + chunk] = run[warp][e];
+    __syncwarp();
+  }
+  grid.sync();
+
+  // scan over chunks, per expert (256 chunk counts loaded together per round)
+  for (int e = gw; e < E; e += nw) {
     int running = 0;
     const int32_t* row = cnt + (int64_t)e * nchunks;
     int32_t* brow = base + (int64_t)e * nchunks;
-    // 256 chunks per round: their counts are loaded together, then scanned 32 at a time
     for (int c0 = 0; c0 < nchunks; c0 += 256) {
       int v[8];
 #pragma unroll
@@ -80,11 +100,15 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
         running += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
     }
-    if (lane == 0) s_cnt[e] = running;
+    if (lane == 0) counts[e] = running;
   }
+  grid.sync();
+
+  // every block: the expert-level scan (offsets and 128-padded offsets)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = __ldcg(counts + e);
   __syncthreads();
   if (warp == 0) {
-    int run = 0, prun = 0;
+    int rsum = 0, prun = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       const int v = e < E ? s_cnt[e] : 0;
@@ -97,64 +121,74 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
         if (lane >= d) { incl += t; pincl += pt; }
       }
       if (e < E) {
-        counts[e] = v;
-        offsets[e] = run + incl - v;
-        padded_offsets[e] = prun + pincl - pv;
+        s_poff[e] = prun + pincl - pv;
+        if (blockIdx.x == 0) {
+          offsets[e] = rsum + incl - v;
+          padded_offsets[e] = prun + pincl - pv;
+        }
       }
-      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      rsum += __shfl_sync(0xFFFFFFFFu, incl, 31);
       prun += __shfl_sync(0xFFFFFFFFu, pincl, 31);
     }
     if (lane == 0) {
-      offsets[E] = run;
-      padded_offsets[E] = prun;
+      s_poff[E] = prun;
+      if (blockIdx.x == 0) {
+        offsets[E] = rsum;
+        padded_offsets[E] = prun;
+      }
     }
   }
-}
+  __syncthreads();
 
-__global__ void __launch_bounds__(kRouteWarps * 32) route_place_kernel(
-    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t P, int topk, int E, int off,
-    const int32_t* __restrict__ base, int nchunks, const int32_t* __restrict__ padded_offsets,
-    int32_t* __restrict__ slot_token, float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot,
-    int64_t capacity, int32_t* status) {
-  __shared__ int run[kRouteWarps][kMaxExperts];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int chunk = blockIdx.x * kRouteWarps + warp;
-  if (chunk >= nchunks) return;
-  for (int e = lane; e < E; e += 32)
-    run[warp][e] = __ldg(padded_offsets + e) + base[(int64_t)e * nchunks + chunk];
-  __syncwarp();
-  const int64_t base_idx = (int64_t)chunk * kRouteChunk;
+  // place
   const unsigned lower = (1u << lane) - 1u;
-  // the chunk's experts and weights, loaded together
-  int loc[kRouteChunk / 32];
-  float wt[kRouteChunk / 32];
-#pragma unroll
-  for (int g = 0; g < kRouteChunk / 32; ++g) {
-    const int64_t idx = base_idx + g * 32 + lane;
-    loc[g] = local_expert(ids, idx, P, off, E);
-    wt[g] = idx < P ? __ldg(w + idx) : 0.0f;
-  }
-#pragma unroll
-  for (int g = 0; g < kRouteChunk / 32; ++g) {
-    const int64_t idx = base_idx + g * 32 + lane;
-    const int l = loc[g];
-    const unsigned grp = __match_any_sync(0xFFFFFFFFu, l);
-    int slot = -1;
-    if (l >= 0) slot = run[warp][l] + __popc(grp & lower);
+  for (int chunk = gw; chunk < nchunks; chunk += nw) {
+    for (int e = lane; e < E; e += 32) run[warp][e] = s_poff[e] + __ldcg(base + (int64_t)e * nchunks + chunk);
     __syncwarp();
-    if (l >= 0 && lane == __ffs(grp) - 1) run[warp][l] += __popc(grp);
-    __syncwarp();
-    if (idx < P) {
-      if (slot >= capacity) {
-        set_status(status, MOE_ERR_DEVICE_INDEX);
-        slot = -1;
-      }
-      pair_slot[idx] = slot;
-      if (slot >= 0) {
-        slot_token[slot] = (int32_t)(idx / topk);
-        slot_weight[slot] = wt[g];
+    const int64_t base_idx = (int64_t)chunk * kRouteChunk;
+    int loc[kRouteChunk / 32];
+    float wt[kRouteChunk / 32];
+#pragma unroll
+    for (int g = 0; g < kRouteChunk / 32; ++g) {
+      const int64_t idx = base_idx + g * 32 + lane;
+      loc[g] = local_expert(ids, idx, P, off, E);
+      wt[g] = idx < P ? __ldg(w + idx) : 0.0f;
+    }
+#pragma unroll
+    for (int g = 0; g < kRouteChunk / 32; ++g) {
+      const int64_t idx = base_idx + g * 32 + lane;
+      const int l = loc[g];
+      const unsigned grp = __match_any_sync(0xFFFFFFFFu, l);
+      int slot = -1;
+      if (l >= 0) slot = run[warp][l] + __popc(grp & lower);
+      __syncwarp();
+      if (l >= 0 && lane == __ffs(grp) - 1) run[warp][l] += __popc(grp);
+      __syncwarp();
+      if (idx < P) {
+        if (slot >= capacity) {
+          set_status(status, MOE_ERR_DEVICE_INDEX);
+          slot = -1;
+        }
+        pair_slot[idx] = slot;
+        if (slot >= 0) {
+          slot_token[slot] = (int32_t)(idx / topk);
+          slot_weight[slot] = wt[g];
+        }
       }
     }
+    __syncwarp();
+  }
+
+  // padding slots: the tail of each expert's padded range, then everything past the last
+  for (int e = gw; e < E; e += nw)
+    for (int p = s_poff[e] + s_cnt[e] + lane; p < s_poff[e + 1] && p < capacity; p += 32) {
+      slot_token[p] = -1;
+      slot_weight[p] = 0.0f;
+    }
+  for (int64_t p = s_poff[E] + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < capacity;
+       p += (int64_t)gridDim.x * blockDim.x) {
+    slot_token[p] = -1;
+    slot_weight[p] = 0.0f;
   }
 }
 
@@ -359,16 +393,30 @@ cudaError_t launch_route(const int32_t* ids, const float* w, int64_t P, int topk
                                                               capacity, status);
     return cudaGetLastError();
   }
-  cudaError_t e = cudaMemsetAsync(slot_token, 0xFF, capacity * sizeof(int32_t), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(slot_weight, 0, capacity * sizeof(float), st);
-  if (e != cudaSuccess) return e;
-  const int blocks = (nchunks + kRouteWarps - 1) / kRouteWarps;
-  if (nchunks > 0) route_count_kernel<<<blocks, kRouteWarps * 32, 0, st>>>(ids, P, E, off, cnt, nchunks);
-  route_scan_kernel<<<1, 1024, 0, st>>>(cnt, nchunks, E, base, counts, offsets, padded_offsets);
-  if (nchunks > 0)
-    route_place_kernel<<<blocks, kRouteWarps * 32, 0, st>>>(ids, w, P, topk, E, off, base, nchunks, padded_offsets,
-                                                           slot_token, slot_weight, pair_slot, capacity, status);
-  return cudaGetLastError();
+  // one cooperative launch: as many blocks as fit on the GPU at once (at most one per
+  // group of kRouteWarps chunks)
+  static PerDeviceInt resident;
+  const int max_blocks = resident.get([] {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_fused_kernel, kRouteWarps * 32, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
+      return 0;
+    return per_sm * sm_count_of_current_device();
+  });
+  if (max_blocks <= 0) return cudaErrorCooperativeLaunchTooLarge;
+  const int blocks = std::max(1, std::min(max_blocks, (nchunks + kRouteWarps - 1) / kRouteWarps));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kRouteWarps * 32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_fused_kernel, ids, w, P, topk, E, off, cnt, base, nchunks, counts, offsets,
+                            padded_offsets, slot_token, slot_weight, pair_slot, capacity, status);
 }
 
 }  // namespace moe
