@@ -49,6 +49,17 @@ NCU_TRAFFIC = {
         "kernel_sources": ("gemm_stream.cu", "pipeline.cuh", "tcgen05.cuh", "common.cuh"),
         "sources_sha256_16": "e2703825511dc62a",
     },
+    ("prefill", "auto", "gemm_l1"): {
+        "bytes": 837389824 + 105923072,
+        "kernel_sources": ("gemm.cu", "gemm_tiled.cuh", "tcgen05.cuh", "kernels.cuh", "common.cuh"),
+        "sources_sha256_16": "9c2d75a51e873869",
+    },
+    ("prefill", "auto", "gemm_l2"): {
+        "bytes": 457888768 + 488578816,
+        "kernel_sources": ("gemm_pair.cu", "gemm_tiled.cuh", "pipeline.cuh", "tcgen05.cuh", "kernels.cuh",
+                           "common.cuh"),
+        "sources_sha256_16": "ed7ec1b3e2d9ee91",
+    },
 }
 
 

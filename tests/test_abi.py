@@ -107,17 +107,21 @@ def test_bench_traffic_is_keyed_by_workload_policy_and_kernel_sources():
     """The ncu DRAM figure belongs to one kernel on one workload: other workloads,
     policies or stages get none, and an edit to the kernel's sources drops it."""
     import bench
-    (wl, pol, stage), tr = next(iter(bench.NCU_TRAFFIC.items()))
-    assert bench.ncu_traffic("prefill", pol, stage) is None
-    assert bench.ncu_traffic(wl, "tiled", stage) is None
-    assert bench.ncu_traffic(wl, pol, "gemm_l2") is None
-    saved = dict(tr)
-    try:
-        tr["sources_sha256_16"] = "0" * 16
-        assert bench.ncu_traffic(wl, pol, stage) is None
-    finally:
-        tr.clear()
-        tr.update(saved)
+    for (wl, pol, stage), tr in bench.NCU_TRAFFIC.items():
+        other_wl = "skew_top8" if wl != "skew_top8" else "prefill"
+        assert (other_wl, pol, stage) not in bench.NCU_TRAFFIC
+        assert bench.ncu_traffic(other_wl, pol, stage) is None
+        assert bench.ncu_traffic(wl, "tiled1", stage) is None
+        assert bench.ncu_traffic(wl, pol, "route") is None
+        saved = dict(tr)
+        try:
+            tr["sources_sha256_16"] = bench.kernel_sources_hash(tr["kernel_sources"])
+            assert bench.ncu_traffic(wl, pol, stage) == tr["bytes"]
+            tr["sources_sha256_16"] = "0" * 16
+            assert bench.ncu_traffic(wl, pol, stage) is None
+        finally:
+            tr.clear()
+            tr.update(saved)
 
 
 def test_bench_rejects_throttled_or_locked_clocks():
