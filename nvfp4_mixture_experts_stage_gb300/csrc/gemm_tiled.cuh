@@ -141,9 +141,13 @@ MOE_DEV void epilogue_load(uint32_t taddr, int half, float (&v)[BN / 2]) {
 // The epilogue math of this thread's row (slot row prow of expert e, n-tile n) for the
 // accumulator half in v.  valid = the row holds a routed pair (padding rows compute but
 // store nothing).  amax collects max |h| of valid rows (L1 SiLU with a dynamic scale).
+// The accumulator is already released when this runs, so it overlaps the next tile's
+// MMAs; store_gap_ns > 0 spreads the BF16 row stores of L2 over that time (a sleep
+// between 16-column chunks): issued in one burst they slow the MMA thread and the
+// copiers that share the SM (measured on the prefill L2: 4 % faster with 350 ns gaps).
 template <int KIND, int BN>
 MOE_DEV void epilogue_store(const GemmParams& p, const float (&v)[BN / 2], int e, int n, int half, bool valid,
-                            int64_t prow, float& amax) {
+                            int64_t prow, float& amax, unsigned store_gap_ns = 0) {
   constexpr bool kL1 = KIND <= kL1Requant;
   constexpr int kCols = BN / 2;
   if constexpr (kL1) {
@@ -235,6 +239,7 @@ MOE_DEV void epilogue_store(const GemmParams& p, const float (&v)[BN / 2], int e
     }
 #pragma unroll
     for (int c = 0; c < kCols / 16; ++c) {
+      if (KIND == kL2Rows && store_gap_ns && c) __nanosleep(store_gap_ns);
       float y[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) y[i] = round_bf16(__fmul_rn(alpha, v[16 * c + i]));
@@ -274,5 +279,10 @@ MOE_DEV void epilogue_finish(const GemmParams& p, float amax) {
 moe_status launch_pair_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                             cudaStream_t st, bool pdl);
 bool pair_gemm_enabled(bool l1);
+
+// Gap between an L2 epilogue warp's 16-column store chunks: a tile's MMAs take about
+// 0.45 us per 256-deep k-block, and the eight chunks with their gaps must end well
+// within that (prefill: 12 k-blocks, 360 ns gaps, 2.5 us of a 5.5 us tile).
+MOE_DEV unsigned l2_store_gap_ns(int nkb) { return (unsigned)min(30 * nkb, 400); }
 
 }  // namespace moe
