@@ -244,8 +244,9 @@ def kernels_per_step(T, topk, dynamic_h):
     """Kernels one moe_forward launches (x's scale derived from the data, as timed here).
 
     T*topk <= 8192: prologue (routing + amax partials + output zeroing), quantize, L1, [requant], L2, cast.
-    Above: count, scan, place, amax, quantize, L1, [requant], L2, cast (the memsets are copies, not kernels)."""
-    n = 5 if T * topk <= SMALL_ROUTE_PAIRS_MAX else 8
+    Above: cooperative routing, amax, quantize, L1, [requant], L2, combine or cast (a memset of the fp32
+    output, where one is used, is a copy, not a kernel)."""
+    n = 5 if T * topk <= SMALL_ROUTE_PAIRS_MAX else 6
     return n + (1 if dynamic_h else 0)
 
 
