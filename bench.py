@@ -50,15 +50,15 @@ NCU_TRAFFIC = {
         "sources_sha256_16": "82cd5229e642c837",
     },
     ("prefill", "auto", "gemm_l1"): {
-        "bytes": 837395200 + 105627136,
+        "bytes": 837395712 + 106525696,
         "kernel_sources": ("gemm.cu", "gemm_tiled.cuh", "tcgen05.cuh", "kernels.cuh", "common.cuh"),
-        "sources_sha256_16": "1ab22b9e52fd26eb",
+        "sources_sha256_16": "8f7efdb0a1ec8f76",
     },
     ("prefill", "auto", "gemm_l2"): {
-        "bytes": 457888768 + 488578816,
+        "bytes": 458552832 + 487683328,
         "kernel_sources": ("gemm_pair.cu", "gemm_tiled.cuh", "pipeline.cuh", "tcgen05.cuh", "kernels.cuh",
                            "common.cuh"),
-        "sources_sha256_16": "ed7ec1b3e2d9ee91",
+        "sources_sha256_16": "cf22ce47f9f3b675",
     },
 }
 
