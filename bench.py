@@ -50,15 +50,15 @@ NCU_TRAFFIC = {
         "sources_sha256_16": "82cd5229e642c837",
     },
     ("prefill", "auto", "gemm_l1"): {
-        "bytes": 837395712 + 106525696,
+        "bytes": 837392128 + 105943296,
         "kernel_sources": ("gemm.cu", "gemm_tiled.cuh", "tcgen05.cuh", "kernels.cuh", "common.cuh"),
-        "sources_sha256_16": "8f7efdb0a1ec8f76",
+        "sources_sha256_16": "a8a5f97754859aa3",
     },
     ("prefill", "auto", "gemm_l2"): {
-        "bytes": 458552832 + 487683328,
+        "bytes": 458279680 + 487261696,
         "kernel_sources": ("gemm_pair.cu", "gemm_tiled.cuh", "pipeline.cuh", "tcgen05.cuh", "kernels.cuh",
                            "common.cuh"),
-        "sources_sha256_16": "cf22ce47f9f3b675",
+        "sources_sha256_16": "dccabab80458f99f",
     },
 }
 

@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s.tempty);  // accumulator free: values are in registers
-      epilogue_store<KIND, BN>(p, v, e, n, half, valid, prow, amax, l2_store_gap_ns(nkb));
+      epilogue_store<KIND, BN>(p, v, e, n, half, valid, prow, amax, epilogue_gap_ns<KIND>(nkb));
     }
     epilogue_finish<KIND>(p, amax);
   }

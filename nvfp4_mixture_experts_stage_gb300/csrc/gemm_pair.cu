@@ -299,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         else
           mbar_arrive_remote(tempty_leader);
       }
-      epilogue_store<KIND, 256>(p, v, e, n, half, valid, prow, amax, l2_store_gap_ns(nkb));
+      epilogue_store<KIND, 256>(p, v, e, n, half, valid, prow, amax, epilogue_gap_ns<KIND>(nkb));
     }
     epilogue_finish<KIND>(p, amax);
   }

@@ -142,12 +142,14 @@ MOE_DEV void epilogue_load(uint32_t taddr, int half, float (&v)[BN / 2]) {
 // accumulator half in v.  valid = the row holds a routed pair (padding rows compute but
 // store nothing).  amax collects max |h| of valid rows (L1 SiLU with a dynamic scale).
 // The accumulator is already released when this runs, so it overlaps the next tile's
-// MMAs; store_gap_ns > 0 spreads the BF16 row stores of L2 over that time (a sleep
-// between 16-column chunks): issued in one burst they slow the MMA thread and the
-// copiers that share the SM (measured on the prefill L2: 4 % faster with 350 ns gaps).
+// MMAs; gap_ns > 0 spreads the work over that time (a sleep between 16-column chunks):
+// issued in one burst, the epilogue's instructions and stores slow the MMA thread, the
+// producer and the copiers that share the SM's sub-partitions (measured on prefill: L2
+// 4 % faster with 360 ns gaps, L1 2 % with 300 ns; gaps that make the epilogue longer
+// than a tile cost far more).
 template <int KIND, int BN>
 MOE_DEV void epilogue_store(const GemmParams& p, const float (&v)[BN / 2], int e, int n, int half, bool valid,
-                            int64_t prow, float& amax, unsigned store_gap_ns = 0) {
+                            int64_t prow, float& amax, unsigned gap_ns = 0) {
   constexpr bool kL1 = KIND <= kL1Requant;
   constexpr int kCols = BN / 2;
   if constexpr (kL1) {
@@ -161,6 +163,7 @@ MOE_DEV void epilogue_store(const GemmParams& p, const float (&v)[BN / 2], int e
     uint32_t sfw = 0;
 #pragma unroll
     for (int c = 0; c < G / 16; ++c) {
+      if (gap_ns && c) __nanosleep(gap_ns);
       float g[16], u[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -239,7 +242,7 @@ MOE_DEV void epilogue_store(const GemmParams& p, const float (&v)[BN / 2], int e
     }
 #pragma unroll
     for (int c = 0; c < kCols / 16; ++c) {
-      if (KIND == kL2Rows && store_gap_ns && c) __nanosleep(store_gap_ns);
+      if (KIND == kL2Rows && gap_ns && c) __nanosleep(gap_ns);
       float y[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) y[i] = round_bf16(__fmul_rn(alpha, v[16 * c + i]));
@@ -280,9 +283,13 @@ moe_status launch_pair_gemm(int kind, const CUtensorMap& ta, const CUtensorMap& 
                             cudaStream_t st, bool pdl);
 bool pair_gemm_enabled(bool l1);
 
-// Gap between an L2 epilogue warp's 16-column store chunks: a tile's MMAs take about
-// 0.45 us per 256-deep k-block, and the eight chunks with their gaps must end well
-// within that (prefill: 12 k-blocks, 360 ns gaps, 2.5 us of a 5.5 us tile).
-MOE_DEV unsigned l2_store_gap_ns(int nkb) { return (unsigned)min(30 * nkb, 400); }
+// Gap between an epilogue warp's 16-column chunks: a tile's MMAs take about 0.45 us per
+// 256-deep k-block, and the chunks with their gaps must end well within that (prefill L2:
+// 12 k-blocks, seven 360 ns gaps, 2.5 us of a 5.5 us tile; L1: 16 k-blocks, three 300 ns
+// gaps beside ~3.4 us of math in a 7.5 us tile).
+template <int KIND>
+MOE_DEV unsigned epilogue_gap_ns(int nkb) {
+  return KIND == kL2Rows ? (unsigned)min(30 * nkb, 400) : KIND == kL1Requant ? (unsigned)min(19 * nkb, 300) : 0u;
+}
 
 }  // namespace moe
