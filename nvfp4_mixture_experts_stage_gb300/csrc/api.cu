@@ -30,6 +30,8 @@ struct Carve {
   }
 };
 
+constexpr int kAmaxMaxBlocks = 4096;  // amax partials of the large-batch layer path
+
 moe_status quantize_launch(int dst, const void* x, int64_t rows, int K, int64_t ld_x, const uint32_t* amax_bits,
                            const float* gs_fixed, float* gs_out, uint8_t* codes, uint8_t* sf,
                            const int32_t* pair_slot, int topk, const int32_t* slot_token, int64_t capacity,
@@ -248,13 +250,14 @@ static size_t forward_layout(Carve& c, int64_t T, int K, int I, int E, int topk,
   parts[11] = c.take<uint8_t>(cap * I / 2);                          // h codes
   parts[12] = c.take<uint8_t>(cap * I / 16);                         // h scales
   parts[13] = c.take<uint8_t>(out_region_bytes(T, K, cap));         // out32, or L2 rows (combine)
+  parts[14] = c.take<uint32_t>(kAmaxMaxBlocks);                      // amax partials (large batches)
   return c.off;
 }
 
 size_t moe_workspace_size(int64_t T_max, int K, int I, int E, int topk) {
   if (T_max < 0 || !shape_ok(K, I, E) || topk < 1 || topk > 32) return 0;
   Carve c{nullptr};
-  void* parts[14];
+  void* parts[15];
   return forward_layout(c, T_max, K, I, E, topk, parts);
 }
 
@@ -418,11 +421,10 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
   if (T == 0) return MOE_OK;
 
   Carve c{reinterpret_cast<uint8_t*>(ws)};
-  void* parts[14];
+  void* parts[15];
   forward_layout(c, T, K, I, E, topk, parts);
   const int64_t cap = moe_slot_capacity(T, topk, E);
   uint32_t* scal = reinterpret_cast<uint32_t*>(parts[0]);
-  uint32_t* x_amax = scal + 0;
   float* h_amax = reinterpret_cast<float*>(scal + 1);
   float* gs_x = reinterpret_cast<float*>(scal + 2);
   const size_t rhalf = moe_route_workspace_size(T, topk, E) / 2;
@@ -488,12 +490,19 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     s = route_impl(topk_ids, topk_w, T, topk, E, expert_offset, counts, offsets, poff, slot_token, slot_weight,
                    pair_slot, cap, rcnt, rbase, dev_status, stream);
     if (s != MOE_OK || (s = mark(stage_events, 1, stream)) != MOE_OK) return s;
+    // the amax of x runs beside the routing (per-block partials, no zeroed word); the
+    // quantiser reduces the partials
+    uint32_t* partials = reinterpret_cast<uint32_t*>(parts[14]);
+    int nparts = 0;
     if (!gs_x_fixed) {
-      s = amax_launch(x, T, K, K, x_amax, stream);
-      if (s != MOE_OK) return s;
+      const int64_t vecs = T * (K / 8);
+      if (vecs >= (int64_t(1) << 32)) return MOE_ERR_UNSUPPORTED_SHAPE;
+      nparts = (int)std::min<int64_t>(std::max<int64_t>(ceil_div(vecs, 256 * 4), 1),
+                                      std::min<int64_t>((int64_t)sm_count() * 8, kAmaxMaxBlocks));
+      if (launch_amax(x, T, K, K, nullptr, nparts, stream, partials, pdl) != cudaSuccess) return MOE_ERR_CUDA;
     }
-    s = quantize_launch(2, x, T, K, K, gs_x_fixed ? nullptr : x_amax, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot,
-                        topk, nullptr, cap, dev_status, stream, nullptr, 0, pdl);
+    s = quantize_launch(2, x, T, K, K, nullptr, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk, nullptr, cap,
+                        dev_status, stream, gs_x_fixed ? nullptr : partials, nparts, pdl);
   }
   if (s != MOE_OK || (s = mark(stage_events, 2, stream)) != MOE_OK) return s;
   if (gs_h_mode == MOE_GS_DYNAMIC) {

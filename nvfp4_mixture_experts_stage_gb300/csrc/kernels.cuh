@@ -33,8 +33,10 @@ struct QuantArgs {
 };
 
 // Host launchers (each translation unit launches its own kernels).
+// partials: each block's maximum to partials[blockIdx.x] instead of an atomic max into
+// *amax_bits; pdl: a programmatic dependent of the previous kernel (see amax_bf16_kernel).
 cudaError_t launch_amax(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, int blocks,
-                        cudaStream_t st);
+                        cudaStream_t st, uint32_t* partials = nullptr, bool pdl = false);
 // pdl: launched as a programmatic dependent of the previous kernel in the stream
 // (only where that kernel and everything before it is known; see moe_forward).
 cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_t st, bool pdl = false);

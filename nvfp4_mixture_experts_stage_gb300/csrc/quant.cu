@@ -20,12 +20,16 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// max |x| over a BF16 matrix -> fp32 bits, atomically max-ed into *amax_bits
-// (must hold 0 or a previous non-negative value on entry).
+// max |x| over a BF16 matrix -> fp32 bits: atomically max-ed into *amax_bits (which must
+// hold 0 or a previous non-negative value on entry), or, with partials, each block's
+// maximum to partials[blockIdx.x] (no zeroed word needed).  It reads only x, so as a
+// programmatic dependent it may run beside the kernel before it; it waits for that
+// kernel only at its end, so a kernel waiting for this one also sees the one before.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint4* __restrict__ x, int64_t T,
                                                         int vec_per_row, int64_t ld_vec,
-                                                        uint32_t* amax_bits) {
+                                                        uint32_t* amax_bits, uint32_t* partials) {
+  griddep_launch_dependents();
   // vector index v -> (row, column); 32-bit division (the host keeps T*vec_per_row < 2^32)
   const uint32_t total = (uint32_t)(T * vec_per_row);
   const uint32_t vpr = (uint32_t)vec_per_row;
@@ -65,8 +69,14 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint4* __restrict_
   if (threadIdx.x < 32) {
     uint32_t v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
     v = __reduce_max_sync(0xFFFFFFFFu, v);
-    if (threadIdx.x == 0 && v) atomicMax(amax_bits, v << 16);  // bf16 -> fp32 bits
+    if (threadIdx.x == 0) {
+      if (partials)
+        partials[blockIdx.x] = v << 16;  // bf16 -> fp32 bits
+      else if (v)
+        atomicMax(amax_bits, v << 16);
+    }
   }
+  griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -355,9 +365,9 @@ cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_
 }
 
 cudaError_t launch_amax(const void* x, int64_t rows, int K, int64_t ld_x, uint32_t* amax_bits, int blocks,
-                        cudaStream_t st) {
-  amax_bf16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), rows, K / 8, ld_x / 8, amax_bits);
-  return cudaGetLastError();
+                        cudaStream_t st, uint32_t* partials, bool pdl) {
+  return launch_ex(amax_bf16_kernel, blocks, 256, 0, st, pdl, reinterpret_cast<const uint4*>(x), rows, K / 8, ld_x / 8,
+                   amax_bits, partials);
 }
 
 // ---------------------------------------------------------------------------
@@ -469,6 +479,17 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
 cudaError_t launch_combine(const void* y, int64_t ld_y, const int32_t* pair_slot, const float* w, int topk, int64_t T,
                            int K, int64_t capacity, void* out, int32_t* status, int blocks, cudaStream_t st,
                            bool pdl) {
+  // no more blocks than are resident at once: a second wave of blocks would start only
+  // as the first ones leave (the loop inside is grid-strided)
+  static PerDeviceInt resident;
+  const int max_blocks = resident.get([] {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_rows_kernel, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    return per_sm * sm_count_of_current_device();
+  });
+  blocks = std::max(1, std::min(blocks, max_blocks));
   return launch_ex(combine_rows_kernel, blocks, 256, 0, st, pdl, reinterpret_cast<const uint4*>(y), ld_y / 8,
                    pair_slot, w, topk, T, K / 8, capacity, reinterpret_cast<uint4*>(out), status);
 }

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_fused_kernel(
     float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot, int64_t capacity, int32_t* status) {
   __shared__ int run[kRouteWarps][kMaxExperts];
   __shared__ int s_cnt[kMaxExperts], s_poff[kMaxExperts + 1];
+  // the layer's next kernel (the amax of x) reads nothing routed and may start now
+  griddep_launch_dependents();
   cg::grid_group grid = cg::this_grid();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kRouteWarps + warp, nw = gridDim.x * kRouteWarps;
