@@ -250,10 +250,13 @@ MOE_DEV void epilogue_store(const GemmParams& p, const float (&v)[BN / 2], int e
       if (KIND == kL2Rows) {
         if (valid) {
           uint4* dy = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_bf16) + prow * p.out_ld + col);
-          dy[0] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                             pack_bf16x2(y[6], y[7]));
-          dy[1] = make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]), pack_bf16x2(y[12], y[13]),
-                             pack_bf16x2(y[14], y[15]));
+          // streaming stores: the rows are read once, by the combine after this kernel;
+          // left as ordinary lines, the last ~100 MB of them would still sit dirty in L2
+          // and be written back while the combine reads
+          __stcs(dy, make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                pack_bf16x2(y[6], y[7])));
+          __stcs(dy + 1, make_uint4(pack_bf16x2(y[8], y[9]), pack_bf16x2(y[10], y[11]), pack_bf16x2(y[12], y[13]),
+                                    pack_bf16x2(y[14], y[15])));
         }
       } else if (tok >= 0) {
         float4* dst = reinterpret_cast<float4*>(p.out32 + (int64_t)tok * p.out_cols + col);
