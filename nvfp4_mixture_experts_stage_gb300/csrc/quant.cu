@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
           sj[j] = -1;
         }
         wj[j] = sj[j] >= 0 ? __ldg(w + t * topk + j) : 0.0f;
-        q[j] = sj[j] >= 0 ? __ldg(y + (int64_t)sj[j] * ld_vec + v) : make_uint4(0, 0, 0, 0);
+        q[j] = sj[j] >= 0 ? __ldcs(y + (int64_t)sj[j] * ld_vec + v) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -471,8 +471,8 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
         add(__ldg(w + t * topk + j), __ldg(y + (int64_t)s * ld_vec + v));
       }
     }
-    out[i] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                        pack_bf16x2(acc[6], acc[7]));
+    __stcs(out + i, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
   }
 }
 
