@@ -91,7 +91,7 @@ moe_status cast_output(const float* out32, void* out_bf16, int64_t T, int K, cud
 
 moe_status combine_rows(const void* y_rows, int64_t ld_y, const int32_t* pair_slot, const float* topk_w, int64_t T,
                         int topk, int K, int64_t capacity, void* out_bf16, int32_t* dev_status, cudaStream_t stream,
-                        bool pdl) {
+                        bool pdl, bool discard_rows = false) {
   if (T < 0 || K <= 0 || K % 8 || topk < 1 || topk > 32 || ld_y < K || ld_y % 8 || capacity < 0)
     return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -100,7 +100,7 @@ moe_status combine_rows(const void* y_rows, int64_t ld_y, const int32_t* pair_sl
   const int64_t n8 = T * K / 8;
   const int blocks = (int)std::min<int64_t>(ceil_div(n8, 256), (int64_t)sm_count() * 8);
   return launch_combine(y_rows, ld_y, pair_slot, topk_w, topk, T, K, capacity, out_bf16, dev_status, blocks, stream,
-                        pdl) == cudaSuccess
+                        pdl, discard_rows) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
@@ -526,7 +526,8 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2, MOE_L2_SCATTER,
                        nullptr, slot_token, slot_weight, out32, T, dev_status, stream, pdl);
   if (s != MOE_OK || (s = mark(stage_events, 5, stream)) != MOE_OK) return s;
-  s = combine ? combine_rows(parts[13], K, pair_slot, topk_w, T, topk, K, cap, out, dev_status, stream, pdl)
+  s = combine ? combine_rows(parts[13], K, pair_slot, topk_w, T, topk, K, cap, out, dev_status, stream, pdl,
+                             true)  // the rows are this call's workspace: dead once combined
               : cast_output(out32, out, T, K, stream, pdl);
   if (s != MOE_OK) return s;
   return mark(stage_events, 6, stream);

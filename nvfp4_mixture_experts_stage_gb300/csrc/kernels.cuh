@@ -43,7 +43,7 @@ cudaError_t launch_quantize(int dst, const QuantArgs& a, int blocks, cudaStream_
 cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st, bool pdl = false);
 cudaError_t launch_combine(const void* y, int64_t ld_y, const int32_t* pair_slot, const float* w, int topk, int64_t T,
                            int K, int64_t capacity, void* out, int32_t* status, int blocks, cudaStream_t st,
-                           bool pdl = false);
+                           bool pdl = false, bool discard_rows = false);
 cudaError_t launch_prepare_weight_sf(const uint8_t* src, uint8_t* dst, int E, int N, int k_sf, int gateup,
                                      int blocks, cudaStream_t st);
 

@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
                                                            const int32_t* __restrict__ pair_slot,
                                                            const float* __restrict__ w, int topk, int64_t T,
                                                            int vec_per_row, int64_t capacity, uint4* __restrict__ out,
-                                                           int32_t* status) {
+                                                           int32_t* status, bool discard_rows) {
   griddep_wait();
   const int64_t total = T * vec_per_row;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -460,6 +460,15 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (sj[j] >= 0) add(wj[j], q[j]);
+      // rows that are dead once read (the layer's own): drop their lines from L2 without
+      // writing them back (the last rows the down GEMM wrote are still dirty there); one
+      // lane per 128 bytes (the launcher asks for it only with 128-byte aligned rows)
+      if (discard_rows && (v & 7) == 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (sj[j] >= 0)
+            asm volatile("discard.global.L2 [%0], 128;" ::"l"(y + (int64_t)sj[j] * ld_vec + v) : "memory");
+      }
     } else {
       for (int j = 0; j < topk; ++j) {
         const int32_t s = __ldg(pair_slot + t * topk + j);
@@ -478,7 +487,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
 
 cudaError_t launch_combine(const void* y, int64_t ld_y, const int32_t* pair_slot, const float* w, int topk, int64_t T,
                            int K, int64_t capacity, void* out, int32_t* status, int blocks, cudaStream_t st,
-                           bool pdl) {
+                           bool pdl, bool discard_rows) {
   // no more blocks than are resident at once: a second wave of blocks would start only
   // as the first ones leave (the loop inside is grid-strided)
   static PerDeviceInt resident;
@@ -491,7 +500,8 @@ cudaError_t launch_combine(const void* y, int64_t ld_y, const int32_t* pair_slot
   });
   blocks = std::max(1, std::min(blocks, max_blocks));
   return launch_ex(combine_rows_kernel, blocks, 256, 0, st, pdl, reinterpret_cast<const uint4*>(y), ld_y / 8,
-                   pair_slot, w, topk, T, K / 8, capacity, reinterpret_cast<uint4*>(out), status);
+                   pair_slot, w, topk, T, K / 8, capacity, reinterpret_cast<uint4*>(out), status,
+                   discard_rows && ld_y % 64 == 0 && (reinterpret_cast<uintptr_t>(y) & 127) == 0);
 }
 
 cudaError_t launch_cast(const float* in, void* out, int64_t n8, int blocks, cudaStream_t st, bool pdl) {
