@@ -50,15 +50,15 @@ NCU_TRAFFIC = {
         "sources_sha256_16": "82cd5229e642c837",
     },
     ("prefill", "auto", "gemm_l1"): {
-        "bytes": 837415168 + 105626880,
+        "bytes": 837366016 + 105961472,
         "kernel_sources": ("gemm.cu", "gemm_tiled.cuh", "tcgen05.cuh", "kernels.cuh", "common.cuh"),
-        "sources_sha256_16": "8f1aa40b4ae7aef9",
+        "sources_sha256_16": "b341981640b064d3",
     },
     ("prefill", "auto", "gemm_l2"): {
-        "bytes": 458495744 + 488831744,
+        "bytes": 458386944 + 488467712,
         "kernel_sources": ("gemm_pair.cu", "gemm_tiled.cuh", "pipeline.cuh", "tcgen05.cuh", "kernels.cuh",
                            "common.cuh"),
-        "sources_sha256_16": "923d42906483f6c5",
+        "sources_sha256_16": "bde3f27492c35604",
     },
 }
 
