@@ -236,7 +236,7 @@ static int64_t out_region_bytes(int64_t T, int K, int64_t cap) {
 
 static size_t forward_layout(Carve& c, int64_t T, int K, int I, int E, int topk, void** parts) {
   const int64_t cap = moe_slot_capacity(T, topk, E);
-  parts[0] = c.take<uint32_t>(512);                                  // scalars, amax partials
+  parts[0] = c.take<uint32_t>(512);                                  // scalars, claim counters, amax partials
   parts[1] = c.take<uint8_t>(moe_route_workspace_size(T, topk, E));  // route tables
   parts[2] = c.take<int32_t>(E);                                     // counts
   parts[3] = c.take<int32_t>(E + 1);                                 // offsets
@@ -443,6 +443,12 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
   uint8_t* h_sf = reinterpret_cast<uint8_t*>(parts[12]);
   float* out32 = reinterpret_cast<float*>(parts[13]);
   const bool combine = use_combine(T, K);  // parts[13] then holds the L2 rows [cap, K] BF16
+  // the weight-streaming GEMMs' tile-claim counters (L1, L2), zeroed by the small-batch
+  // prologue; larger batches walk static ranges (no counter)
+  int32_t* claims = reinterpret_cast<int32_t*>(scal + 8);
+  const bool small = T * topk <= kSmallRoutePairsMax;
+  int32_t* claim_l1 = small ? claims : nullptr;
+  int32_t* claim_l2 = small ? claims + 1 : nullptr;
 
   moe_status s;
   // Kernels after the first run as programmatic dependents of their predecessor (each
@@ -451,8 +457,9 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
   bool pdl = true;
   for (int i = 1; stage_events && i < 6; ++i) pdl = pdl && stage_events[i] == nullptr;
   if (mark(stage_events, 0, stream) != MOE_OK) return MOE_ERR_CUDA;
-  if (T * topk <= kSmallRoutePairsMax) {
-    // one launch: routing (block 0) + per-block amax of x + zeroing of out32
+  if (small) {
+    // one launch: routing (block 0) + per-block amax of x + zeroing of out32 and of the
+    // tile-claim counters
     uint32_t* partials = scal + 256;
     const int64_t vecs = T * (K / 8), n4 = T * K / 4;
     const int nb = (int)std::min<int64_t>(std::max<int64_t>(ceil_div(std::max(vecs, n4), 2048), 1), 256);
@@ -478,6 +485,8 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     pa.amax_partials = gs_x_fixed ? nullptr : partials;
     pa.out32 = combine ? nullptr : out32;
     pa.out32_n4 = combine ? 0 : n4;
+    pa.zero_words = claims;
+    pa.n_zero_words = 2;
     if (launch_forward_prologue(pa, nb, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if ((s = mark(stage_events, 1, stream)) != MOE_OK) return s;
     // Not a programmatic dependent: launched early, its blocks would be placed on the
@@ -508,23 +517,23 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
   if (gs_h_mode == MOE_GS_DYNAMIC) {
     s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
                        w->gs_w1_up, MOE_L1_SILU_BF16, h_bf16, h_amax, nullptr, nullptr, nullptr, dev_status, stream,
-                       pdl);
+                       pdl, claim_l1);
     if (s != MOE_OK || (s = mark(stage_events, 3, stream)) != MOE_OK) return s;
     s = quantize_launch(3, h_bf16, cap, I, I, reinterpret_cast<const uint32_t*>(h_amax), nullptr, gs_h, h_fp4, h_sf,
                         nullptr, 0, slot_token, cap, dev_status, stream, nullptr, 0, pdl);
   } else {
     s = launch_gemm_l1(a_fp4, a_sf, gs_x, offsets, poff, E, cap, K, I, w->w1_fp4, w->w1_sf, w->gs_w1_gate,
                        w->gs_w1_up, MOE_L1_SILU_REQUANT, nullptr, nullptr, h_fp4, h_sf, gs_h, dev_status, stream,
-                       pdl);
+                       pdl, claim_l1);
     if (s != MOE_OK || (s = mark(stage_events, 3, stream)) != MOE_OK) return s;
   }
   if (s != MOE_OK || (s = mark(stage_events, 4, stream)) != MOE_OK) return s;
   if (combine)
     s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2,
-                       MOE_L2_ROWS_BF16, parts[13], nullptr, nullptr, nullptr, T, dev_status, stream, pdl);
+                       MOE_L2_ROWS_BF16, parts[13], nullptr, nullptr, nullptr, T, dev_status, stream, pdl, claim_l2);
   else
     s = launch_gemm_l2(h_fp4, h_sf, gs_h, offsets, poff, E, cap, I, K, w->w2_fp4, w->w2_sf, w->gs_w2, MOE_L2_SCATTER,
-                       nullptr, slot_token, slot_weight, out32, T, dev_status, stream, pdl);
+                       nullptr, slot_token, slot_weight, out32, T, dev_status, stream, pdl, claim_l2);
   if (s != MOE_OK || (s = mark(stage_events, 5, stream)) != MOE_OK) return s;
   s = combine ? combine_rows(parts[13], K, pair_slot, topk_w, T, topk, K, cap, out, dev_status, stream, pdl,
                              true)  // the rows are this call's workspace: dead once combined

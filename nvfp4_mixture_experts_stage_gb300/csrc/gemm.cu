@@ -329,10 +329,10 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
                           const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
                           const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
                           float* h_amax, uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h, int32_t* status,
-                          cudaStream_t st, bool pdl) {
+                          cudaStream_t st, bool pdl, int32_t* tile_claim) {
   if (use_stream_gemm(cap, E, K))
     return launch_stream_gemm_l1(a_fp4, a_sf, gs_a, offsets, padded_offsets, E, cap, K, I, w1_fp4, w1_sf, gs_g, gs_u,
-                                 epilogue, out_bf16, h_amax, h_fp4, h_sf, gs_h, status, st, pdl);
+                                 epilogue, out_bf16, h_amax, h_fp4, h_sf, gs_h, status, st, pdl, tile_claim);
   const int bn = I % 128 == 0 ? 256 : 128;
   CUtensorMap ta, tb, tsb;
   if (!make_tmap(&ta, a_fp4, (uint64_t)K / 2, (uint64_t)cap, kBM)) return MOE_ERR_CUDA;
@@ -385,10 +385,10 @@ moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float
                           const int32_t* padded_offsets, int E, int64_t cap, int I, int K, const uint8_t* w2_fp4,
                           const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
                           const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
-                          int32_t* status, cudaStream_t st, bool pdl) {
+                          int32_t* status, cudaStream_t st, bool pdl, int32_t* tile_claim) {
   if (use_stream_gemm(cap, E, I))
     return launch_stream_gemm_l2(h_fp4, h_sf, gs_h, offsets, padded_offsets, E, cap, I, K, w2_fp4, w2_sf, gs_w2,
-                                 epilogue, y_rows, slot_token, slot_weight, out32, T, status, st, pdl);
+                                 epilogue, y_rows, slot_token, slot_weight, out32, T, status, st, pdl, tile_claim);
   const int bn = K % 256 == 0 ? 256 : 128;
   const bool pair = bn == 256 && pair_gemm_enabled(false);
   CUtensorMap ta, tb, tsb;

@@ -14,6 +14,12 @@
 //     weight-scale atoms it brings (the tiled kernel copies eight);
 //   * each CTA walks a contiguous range of (expert, chunk, weight-block) tiles, so
 //     consecutive tiles reuse the resident activation scales;
+//   * when the launch is given a claim counter (zeroed by an earlier kernel of the
+//     layer), the last tiles (three per CTA) are not in any range: every CTA claims
+//     them one at a time once its range is done, so CTAs that started late (behind
+//     the previous GEMM's slowest CTA) or stream slower take fewer of them.  The
+//     producer claims and passes each tile to the other roles through a small queue
+//     in shared memory;
 //   * warp 6 builds the TMEM images of the next chunk's activation scales in shared
 //     memory while the current chunk runs;
 //   * two MMA-issuing warps split every tile's k-blocks by parity into two
@@ -88,7 +94,11 @@ struct Params {
   int64_t cap;
   int32_t* status;
   int early_weights;                // request weights before griddep_wait (see the producer)
+  int32_t* claim;                   // pool claim counter, zero at launch; NULL: static ranges only
 };
+
+constexpr int kTileQ = 8;            // queue of claimed tiles (the producer leads the epilogue by <= 4)
+constexpr int kPoolPerCta = 3;       // pool size in tiles per CTA
 
 template <int CHUNK>
 struct __align__(1024) Smem {
@@ -108,6 +118,10 @@ struct __align__(1024) Smem {
   uint64_t img_full;
   uint64_t img_free;
   uint64_t dep;                     // the producer's griddep_wait() has returned
+  uint64_t tq_full[kTileQ];         // entry written (the producer)
+  uint64_t tq_empty[kTileQ];        // entry read by the four consumer roles
+  int tq[kTileQ];                   // claimed tiles in claim order; -1 ends the walk
+  int epi_tile;                     // the epilogue warps' copy of the entry being read
   uint32_t tmem_base;
   int abort_flag;
   int bad_offsets;
@@ -133,6 +147,65 @@ struct Cursor {
 };
 
 MOE_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Barrier of the four epilogue warps that also returns whether any of them passed true,
+// so that all of them take the same branch.
+MOE_DEV bool epi_bar_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+// The tiles of one CTA: its static range [t, hi), then (dyn) the tiles it claims from
+// the pool.  The producer claims each pool tile and writes it into queue entry d % kTileQ;
+// the issuers, the scale-image builder and the epilogue each read every entry in order
+// (one thread per role waits and arrives).  An entry of -1 ends the walk.
+struct TileWalk {
+  int t, hi;
+  int d = 0;
+  bool dyn;
+};
+
+template <class S>
+MOE_DEV int claim_tile(TileWalk& w, S& s, const Params& p, int n_static, int total, int* abort_flag, bool& ok) {
+  if (w.t < w.hi) return w.t++;
+  if (!w.dyn) return -1;
+  const int q = w.d % kTileQ;
+  if (!wait_bar_bounded(&s.tq_empty[q], ((uint32_t)(w.d / kTileQ) & 1) ^ 1, abort_flag, p.status)) {
+    ok = false;
+    return -1;
+  }
+  int v = n_static + atomicAdd(p.claim, 1);
+  if (v >= total) {
+    v = -1;
+    w.dyn = false;
+  }
+  s.tq[q] = v;
+  mbar_arrive(&s.tq_full[q]);
+  ++w.d;
+  return v;
+}
+
+// One thread of a consumer role: the next tile, or -1 (walk over, or aborted).
+template <class S>
+MOE_DEV int next_tile(TileWalk& w, S& s, int* abort_flag, int32_t* status) {
+  if (w.t < w.hi) return w.t++;
+  if (!w.dyn) return -1;
+  const int q = w.d % kTileQ;
+  if (!wait_bar_bounded(&s.tq_full[q], (uint32_t)(w.d / kTileQ) & 1, abort_flag, status)) {
+    w.dyn = false;
+    return -1;
+  }
+  const int v = *reinterpret_cast<volatile int*>(&s.tq[q]);
+  mbar_arrive(&s.tq_empty[q]);
+  ++w.d;
+  if (v < 0) w.dyn = false;
+  return v;
+}
 
 template <int KIND, int CHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -196,6 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.img_full, 1);
     mbar_init(&s.img_free, 2);
     mbar_init(&s.dep, 1);
+    for (int i = 0; i < kTileQ; ++i) {
+      mbar_init(&s.tq_full[i], 1);
+      mbar_init(&s.tq_empty[i], 4);
+    }
     s.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -215,8 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool bad = s.bad_offsets != 0;
   if (bad && threadIdx.x == 0) set_status(p.status, MOE_ERR_DEVICE_INDEX);
   const int total = bad ? 0 : s.cum[p.E];
-  const int t_lo = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
-  const int t_hi = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  const int n_static = p.claim ? max(0, total - kPoolPerCta * (int)gridDim.x) : total;
+  const int t_lo = (int)(((int64_t)n_static * blockIdx.x) / gridDim.x);
+  const int t_hi = (int)(((int64_t)n_static * (blockIdx.x + 1)) / gridDim.x);
+  const bool dyn = p.claim != nullptr && n_static < total;
   const int nkb = (p.Kred + 255) >> 8;
   const int ksf4 = p.Kred >> 6;  // k-steps (scale atoms per 128 rows)
   // both issuers take k-blocks only when a tile has an even number of them (with the
@@ -262,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < j; ++i) tma_load_2d(s.b[i], &tmap_x, &s.full[i], (i % nkb) * 128, pre_row[i]);
       };
       Cursor<CHUNK> cur;
-      for (int t = t_lo; t < t_hi && ok; ++t) {
+      TileWalk walk{t_lo, t_hi, 0, dyn};
+      for (int t; ok && (t = claim_tile(walk, s, p, n_static, total, abort_flag, ok)) >= 0;) {
         int c, n;
         cur.locate(s, p.n_tiles, t, c, n);
         const int e = cur.e;
@@ -311,7 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dw0 = sdesc_sw128(s.w[0]), db0 = sdesc_sw128(s.b[0]);
       const uint64_t dsf0 = sdesc_sf(s.sfw[0]), dimg0 = sdesc_sf(s.img[0]);
       Cursor<CHUNK> cur;
-      for (int t = t_lo; t < t_hi && ok; ++t, ++it, g += nkb) {
+      TileWalk walk{t_lo, t_hi, 0, dyn};
+      for (int t; ok && (t = next_tile(walk, s, abort_flag, p.status)) >= 0; ++it, g += nkb) {
         int c, n;
         cur.locate(s, p.n_tiles, t, c, n);
         bool fresh = false;  // first tile of a chunk: copy this issuer's activation scales
@@ -387,7 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < ksf4; ++k) *reinterpret_cast<uint4*>(&s.img[k][lane * 16]) = make_uint4(0u, 0u, 0u, 0u);
     int ch = -1, last_e = -1, last_c = -1;
     Cursor<CHUNK> cur;
-    for (int t = t_lo; t < t_hi; ++t) {
+    TileWalk walk{t_lo, t_hi, 0, dyn};
+    for (;;) {
+      int t = 0;
+      if (lane == 0) t = next_tile(walk, s, abort_flag, p.status);
+      t = __shfl_sync(0xFFFFFFFFu, t, 0);
+      if (t < 0) break;
       int c, n;
       cur.locate(s, p.n_tiles, t, c, n);
       if (cur.e == last_e && c == last_c) continue;
@@ -418,7 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     Cursor<CHUNK> cur;
     float amax = 0.0f;
-    for (int t = t_lo; t < t_hi; ++t, ++it) {
+    TileWalk walk{t_lo, t_hi, 0, dyn};
+    for (;; ++it) {
+      int t;
+      if (walk.t < walk.hi) {
+        t = walk.t++;
+      } else if (!walk.dyn) {
+        t = -1;
+      } else {  // one thread reads the queue entry for the four warps
+        if (tid == 0) s.epi_tile = next_tile(walk, s, abort_flag, p.status);
+        epi_bar();
+        t = *reinterpret_cast<volatile int*>(&s.epi_tile);
+        if (t < 0) walk.dyn = false;
+      }
+      if (t < 0) break;
       int c, n;
       cur.locate(s, p.n_tiles, t, c, n);
       const int e = cur.e;
@@ -437,8 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int buf = it % kAccBufs;
       wait_bar_bounded(&s.tfull[buf], (uint32_t)(it / kAccBufs) & 1, abort_flag, p.status);
-      epi_bar();  // every epilogue warp has arrived (and sees an abort set before)
-      if (*(volatile int*)abort_flag) break;
+      // every epilogue warp has arrived; all of them leave if any of them saw an abort
+      if (epi_bar_any(*(volatile int*)abort_flag != 0)) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + 2 * buf * kChunk;
       float v[kChunk];
@@ -609,7 +708,8 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
                                  const int32_t* padded_offsets, int E, int64_t cap, int K, int I,
                                  const uint8_t* w1_fp4, const uint8_t* w1_sf, const float* gs_g, const float* gs_u,
                                  int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4, uint8_t* h_sf,
-                                 const float* gs_h, int32_t* status, cudaStream_t st, bool pdl) {
+                                 const float* gs_h, int32_t* status, cudaStream_t st, bool pdl,
+                                 int32_t* tile_claim) {
   using namespace stream;
   const int chunk = stream_chunk(cap, E);
   CUtensorMap tw, tx;
@@ -636,6 +736,7 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
   p.gs_h = gs_h;
   p.cap = cap;
   p.status = status;
+  p.claim = tile_claim;
   if (epilogue == MOE_L1_SILU_BF16 && h_amax) {
     if (cudaMemsetAsync(h_amax, 0, sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
     pdl = false;  // the predecessor is now the memset, not a kernel
@@ -652,7 +753,7 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
                                  const int32_t* padded_offsets, int E, int64_t cap, int I, int K,
                                  const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2, int epilogue,
                                  void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
-                                 int64_t T, int32_t* status, cudaStream_t st, bool pdl) {
+                                 int64_t T, int32_t* status, cudaStream_t st, bool pdl, int32_t* tile_claim) {
   using namespace stream;
   const int chunk = stream_chunk(cap, E);
   CUtensorMap tw, tx;
@@ -680,6 +781,7 @@ moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, cons
   p.out_cols = K;
   p.cap = cap;
   p.status = status;
+  p.claim = tile_claim;
   switch (epilogue) {
     case MOE_L2_ROWS_BF16: return launch_kind<kL2Rows>(tw, tx, p, chunk, st, pdl);
     case MOE_L2_SCATTER: return launch_kind<kL2Scatter>(tw, tx, p, chunk, st, pdl);

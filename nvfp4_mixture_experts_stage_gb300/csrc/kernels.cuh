@@ -80,6 +80,8 @@ struct PrologueArgs {
   uint32_t* amax_partials;   // [amax_blocks] fp32 bits, or NULL (fixed global scale)
   float* out32;
   int64_t out32_n4;          // float4 count to zero
+  int32_t* zero_words;       // words block 0 zeroes (the GEMMs' tile-claim counters), or NULL
+  int n_zero_words;
 };
 cudaError_t launch_forward_prologue(const PrologueArgs& a, int amax_blocks, cudaStream_t st);
 
@@ -88,12 +90,12 @@ moe_status launch_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, const float
                           const int32_t* padded_offsets, int E, int64_t cap, int K, int I, const uint8_t* w1_fp4,
                           const uint8_t* w1_sf, const float* gs_g, const float* gs_u, int epilogue, void* out_bf16,
                           float* h_amax, uint8_t* h_fp4, uint8_t* h_sf, const float* gs_h, int32_t* status,
-                          cudaStream_t st, bool pdl = false);
+                          cudaStream_t st, bool pdl = false, int32_t* tile_claim = nullptr);
 moe_status launch_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
                           const int32_t* padded_offsets, int E, int64_t cap, int I, int K, const uint8_t* w2_fp4,
                           const uint8_t* w2_sf, const float* gs_w2, int epilogue, void* y_rows,
                           const int32_t* slot_token, const float* slot_weight, float* out32, int64_t T,
-                          int32_t* status, cudaStream_t st, bool pdl = false);
+                          int32_t* status, cudaStream_t st, bool pdl = false, int32_t* tile_claim = nullptr);
 
 // ---- gemm_stream.cu (weight-streaming kernel for small per-expert slot counts) ----
 bool stream_gemm_supported(int Kred);
@@ -101,12 +103,14 @@ moe_status launch_stream_gemm_l1(const uint8_t* a_fp4, const uint8_t* a_sf, cons
                                  const int32_t* padded_offsets, int E, int64_t cap, int K, int I,
                                  const uint8_t* w1_fp4, const uint8_t* w1_sf, const float* gs_g, const float* gs_u,
                                  int epilogue, void* out_bf16, float* h_amax, uint8_t* h_fp4, uint8_t* h_sf,
-                                 const float* gs_h, int32_t* status, cudaStream_t st, bool pdl = false);
+                                 const float* gs_h, int32_t* status, cudaStream_t st, bool pdl = false,
+                                 int32_t* tile_claim = nullptr);
 moe_status launch_stream_gemm_l2(const uint8_t* h_fp4, const uint8_t* h_sf, const float* gs_h, const int32_t* offsets,
                                  const int32_t* padded_offsets, int E, int64_t cap, int I, int K,
                                  const uint8_t* w2_fp4, const uint8_t* w2_sf, const float* gs_w2, int epilogue,
                                  void* y_rows, const int32_t* slot_token, const float* slot_weight, float* out32,
-                                 int64_t T, int32_t* status, cudaStream_t st, bool pdl = false);
+                                 int64_t T, int32_t* status, cudaStream_t st, bool pdl = false,
+                                 int32_t* tile_claim = nullptr);
 
 // Gate/up scale fold (set-up, quant.cu).
 cudaError_t launch_fold_gate_up(uint8_t* sf, const float* gg, const float* gu, float* common, int E, int I, int K,

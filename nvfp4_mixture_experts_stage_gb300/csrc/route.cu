@@ -325,12 +325,13 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 }
 
 // The start of the layer for small batches, in one launch: block 0 routes (as
-// route_small_kernel); the other blocks take the per-block max |x| (written to
-// amax_partials[block-1], no atomics, so nothing has to be cleared first) and zero
-// the fp32 output accumulator.
+// route_small_kernel) and zeroes the GEMMs' tile-claim counters; the other blocks take
+// the per-block max |x| (written to amax_partials[block-1], no atomics, so nothing has
+// to be cleared first) and zero the fp32 output accumulator.
 __global__ void __launch_bounds__(1024) forward_prologue_kernel(PrologueArgs a) {
   extern __shared__ int sm[];
   if (blockIdx.x == 0) {
+    if (threadIdx.x < a.n_zero_words) a.zero_words[threadIdx.x] = 0;
     route_small_block(a.ids, a.w, a.P, a.topk, a.E, a.off, a.counts, a.offsets, a.padded_offsets, a.slot_token,
                       a.slot_weight, a.pair_slot, a.capacity, a.status, sm);
     return;
