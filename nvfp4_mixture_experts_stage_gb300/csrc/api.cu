@@ -489,10 +489,11 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     pa.n_zero_words = 2;
     if (launch_forward_prologue(pa, nb, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if ((s = mark(stage_events, 1, stream)) != MOE_OK) return s;
-    // Not a programmatic dependent: launched early, its blocks would be placed on the
-    // few SMs the prologue leaves free and run there several times slower.
+    // A programmatic dependent launched only once the prologue's amax blocks have exited
+    // (launched beside them, its blocks were placed on the few SMs they left free and ran
+    // several times slower).
     s = quantize_launch(2, x, T, K, K, nullptr, gs_x_fixed, gs_x, a_fp4, a_sf, pair_slot, topk, nullptr, cap,
-                        dev_status, stream, gs_x_fixed ? nullptr : partials, nb, false);
+                        dev_status, stream, gs_x_fixed ? nullptr : partials, nb, pdl);
   } else {
     if (!combine && cudaMemsetAsync(out32, 0, (size_t)T * K * sizeof(float), stream) != cudaSuccess)
       return MOE_ERR_CUDA;

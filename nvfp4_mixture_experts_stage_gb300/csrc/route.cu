@@ -327,10 +327,16 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 // The start of the layer for small batches, in one launch: block 0 routes (as
 // route_small_kernel) and zeroes the GEMMs' tile-claim counters; the other blocks take
 // the per-block max |x| (written to amax_partials[block-1], no atomics, so nothing has
-// to be cleared first) and zero the fp32 output accumulator.
+// to be cleared first) and zero the fp32 output accumulator.  Only block 0 triggers the
+// dependent launch.
 __global__ void __launch_bounds__(1024) forward_prologue_kernel(PrologueArgs a) {
   extern __shared__ int sm[];
   if (blockIdx.x == 0) {
+    // The quantiser after this kernel is a programmatic dependent: it launches once this
+    // block has passed here and every other block has exited (those blocks never
+    // trigger), so its blocks spread over the SMs the amax blocks have left, and wait
+    // for this block's routing tables in griddep_wait().
+    griddep_launch_dependents();
     if (threadIdx.x < a.n_zero_words) a.zero_words[threadIdx.x] = 0;
     route_small_block(a.ids, a.w, a.P, a.topk, a.E, a.off, a.counts, a.offsets, a.padded_offsets, a.slot_token,
                       a.slot_weight, a.pair_slot, a.capacity, a.status, sm);
