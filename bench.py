@@ -45,20 +45,20 @@ METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 
 # files that kernel is compiled from hash to the captured ones.
 NCU_TRAFFIC = {
     ("decode", "auto", "gemm_l1"): {
-        "bytes": 670468352 + 3644160,
+        "bytes": 670391808 + 3446016,
         "kernel_sources": ("gemm_stream.cu", "pipeline.cuh", "tcgen05.cuh", "common.cuh"),
-        "sources_sha256_16": "82cd5229e642c837",
+        "sources_sha256_16": "a08c905538ddbf33",
     },
     ("prefill", "auto", "gemm_l1"): {
-        "bytes": 837366016 + 105961472,
+        "bytes": 837496064 + 106010112,
         "kernel_sources": ("gemm.cu", "gemm_tiled.cuh", "tcgen05.cuh", "kernels.cuh", "common.cuh"),
-        "sources_sha256_16": "b341981640b064d3",
+        "sources_sha256_16": "1a3b31931dade1e0",
     },
     ("prefill", "auto", "gemm_l2"): {
-        "bytes": 458386944 + 488467712,
+        "bytes": 458433792 + 488067328,
         "kernel_sources": ("gemm_pair.cu", "gemm_tiled.cuh", "pipeline.cuh", "tcgen05.cuh", "kernels.cuh",
                            "common.cuh"),
-        "sources_sha256_16": "bde3f27492c35604",
+        "sources_sha256_16": "7bf5470c29262a83",
     },
 }
 
