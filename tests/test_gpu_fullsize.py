@@ -112,6 +112,42 @@ def test_decode_every_token_dynamic_and_fixed(layer, decode_ref, policy):
         B.moe_set_gemm_policy(old)
 
 
+def test_decode_repeated_calls_claim_every_tile(layer, decode_ref):
+    """Three calls of the decode layer on one workspace.  The weight-streaming GEMMs take
+    their last tiles from claim counters that each call's prologue zeroes; a counter
+    left over from the previous call would drop those tiles from the second call on."""
+    wl = workloads.WORKLOADS["decode"]
+    layer.topk, layer.expert_offset = wl.topk, wl.expert_offset
+    x = workloads.activations(wl).cuda()
+    ids, w = workloads.routing(wl)
+    ids, w = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    fw = R.Forward(layer, wl.T, B.MOE_GS_FIXED)
+    fw.gs_h.fill_(float(decode_ref["gs_h"]))
+    for i in range(3):
+        out = fw(x, ids, w).float().cpu().numpy()
+        assert fw.status.item() == 0
+        assert_layer_close(out, decode_ref["out"], f"decode call {i}")
+
+
+def test_prefill_repeated_calls_bitwise_equal(layer):
+    """The tiled GEMMs and the per-token combine fix every output's summation order
+    (one tile per output, k in order; a token's rows in pair order), so repeated
+    calls give the same bits."""
+    wl = workloads.WORKLOADS["prefill"]
+    layer.topk, layer.expert_offset = wl.topk, wl.expert_offset
+    x = workloads.activations(wl).cuda()
+    ids, w = workloads.routing(wl)
+    ids, w = torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda()
+    fw = R.Forward(layer, wl.T, B.MOE_GS_FIXED)
+    fw.gs_h.fill_(float(workloads.fixed_gs_h(wl)))
+    first = fw(x, ids, w).clone()
+    for _ in range(2):
+        again = fw(x, ids, w)
+        torch.cuda.synchronize()
+        assert fw.status.item() == 0
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+
+
 def _cover_tokens(wl, ids):
     """Tokens whose slots include the last row of every 128-row m-tile of every expert
     (the oracle's slot order), so each tile of both grouped GEMMs has a compared row."""
