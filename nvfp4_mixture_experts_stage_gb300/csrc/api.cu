@@ -487,6 +487,7 @@ moe_status moe_forward_traced(const void* x, int64_t T, int K, int I, int E, con
     pa.out32_n4 = combine ? 0 : n4;
     pa.zero_words = claims;
     pa.n_zero_words = 2;
+    pa.fill_padding = gs_h_mode == MOE_GS_DYNAMIC;
     if (launch_forward_prologue(pa, nb, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if ((s = mark(stage_events, 1, stream)) != MOE_OK) return s;
     // A programmatic dependent launched only once the prologue's amax blocks have exited

@@ -82,6 +82,9 @@ struct PrologueArgs {
   int64_t out32_n4;          // float4 count to zero
   int32_t* zero_words;       // words block 0 zeroes (the GEMMs' tile-claim counters), or NULL
   int n_zero_words;
+  int fill_padding;          // write slot_token -1 / slot_weight 0 into the padding slots (only the
+                             // masked requantisation of h reads them; the GEMMs stop at each
+                             // expert's slot count)
 };
 cudaError_t launch_forward_prologue(const PrologueArgs& a, int amax_blocks, cudaStream_t st);
 

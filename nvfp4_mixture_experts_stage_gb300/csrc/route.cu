@@ -207,7 +207,7 @@ __device__ __forceinline__ void route_small_block(
     const int32_t* __restrict__ ids, const float* __restrict__ w, int P, int topk, int E, int off,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ padded_offsets,
     int32_t* __restrict__ slot_token, float* __restrict__ slot_weight, int32_t* __restrict__ pair_slot,
-    int64_t capacity, int32_t* status, int* wcnt) {
+    int64_t capacity, int32_t* status, int* wcnt, bool fill_padding = true) {
   __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (P + 1023) / 1024;  // groups per warp
@@ -303,6 +303,7 @@ __device__ __forceinline__ void route_small_block(
     }
   }
   // padding slots: the tail of each expert's padded range, then everything past the last
+  if (!fill_padding) return;
   for (int e = warp; e < E; e += 32)
     for (int p = s_poff[e] + s_cnt[e] + lane; p < s_poff[e + 1] && p < capacity; p += 32) {
       slot_token[p] = -1;
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(1024) forward_prologue_kernel(PrologueArgs a) 
     griddep_launch_dependents();
     if (threadIdx.x < a.n_zero_words) a.zero_words[threadIdx.x] = 0;
     route_small_block(a.ids, a.w, a.P, a.topk, a.E, a.off, a.counts, a.offsets, a.padded_offsets, a.slot_token,
-                      a.slot_weight, a.pair_slot, a.capacity, a.status, sm);
+                      a.slot_weight, a.pair_slot, a.capacity, a.status, sm, a.fill_padding != 0);
     return;
   }
   const uint32_t nb = gridDim.x - 1, b = blockIdx.x - 1;
