@@ -644,20 +644,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const float alpha = __fmul_rn(__ldg(p.gs_a), __ldg(p.gs_w0 + e));
         const int col = n * 128 + q * 32 + lane;  // output column
+        if (KIND == kL2Rows) {
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          if (j < cnt_c) {  // uniform across the warp
-            const float y = round_bf16(__fmul_rn(alpha, v[j]));
-            const int64_t prow = row0 + j;
-            if (KIND == kL2Rows) {
-              reinterpret_cast<__nv_bfloat16*>(p.out_bf16)[prow * p.out_ld + col] = __float2bfloat16_rn(y);
-            } else {
-              const int32_t tok = __shfl_sync(0xFFFFFFFFu, tok_l[j >> 5], j & 31);
-              const float wt = __shfl_sync(0xFFFFFFFFu, w_l[j >> 5], j & 31);
-              if (tok >= p.T) {
-                set_status(p.status, MOE_ERR_DEVICE_INDEX);
-              } else if (tok >= 0) {
-                atomicAdd(p.out32 + (int64_t)tok * p.out_cols + col, __fmul_rn(wt, y));
+          for (int j = 0; j < kChunk; ++j) {
+            if (j < cnt_c) {  // uniform across the warp
+              const float y = round_bf16(__fmul_rn(alpha, v[j]));
+              reinterpret_cast<__nv_bfloat16*>(p.out_bf16)[(row0 + j) * p.out_ld + col] = __float2bfloat16_rn(y);
+            }
+          }
+        } else {
+          // Weighted scatter, four slots at a time: lane l holds column col of every slot;
+          // the products are exchanged so that lane l adds columns 4(l%8)..4(l%8)+3 of
+          // slot j0 + l/8 with one vector reduction (a quarter of the atomic operations).
+          const int sub = lane >> 3, c4 = (lane & 7) * 4;
+#pragma unroll
+          for (int j0 = 0; j0 < kChunk; j0 += 4) {
+            if (j0 < cnt_c) {  // uniform across the warp
+              float pr[4];
+              int32_t tk[4];
+#pragma unroll
+              for (int s4 = 0; s4 < 4; ++s4) {
+                const int j = j0 + s4;
+                tk[s4] = __shfl_sync(0xFFFFFFFFu, tok_l[j >> 5], j & 31);
+                const float wt = __shfl_sync(0xFFFFFFFFu, w_l[j >> 5], j & 31);
+                pr[s4] = __fmul_rn(wt, round_bf16(__fmul_rn(alpha, v[j])));
+              }
+              float a[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float x0 = __shfl_sync(0xFFFFFFFFu, pr[0], c4 + i);
+                const float x1 = __shfl_sync(0xFFFFFFFFu, pr[1], c4 + i);
+                const float x2 = __shfl_sync(0xFFFFFFFFu, pr[2], c4 + i);
+                const float x3 = __shfl_sync(0xFFFFFFFFu, pr[3], c4 + i);
+                a[i] = sub == 0 ? x0 : sub == 1 ? x1 : sub == 2 ? x2 : x3;
+              }
+              const int32_t tok = sub == 0 ? tk[0] : sub == 1 ? tk[1] : sub == 2 ? tk[2] : tk[3];
+              if (j0 + sub < cnt_c) {
+                if (tok >= p.T) {
+                  set_status(p.status, MOE_ERR_DEVICE_INDEX);
+                } else if (tok >= 0) {
+                  atomicAdd(reinterpret_cast<float4*>(p.out32 + (int64_t)tok * p.out_cols + n * 128 + q * 32 + c4),
+                            make_float4(a[0], a[1], a[2], a[3]));
+                }
               }
             }
           }
