@@ -31,6 +31,7 @@
 // CTAs running at the same time share weight tiles through L2; the expert of a tile
 // comes from the padded offsets on the device (no host sync).
 #include "gemm_tiled.cuh"
+#include "pipeline.cuh"
 
 namespace moe {
 
@@ -124,9 +125,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[kStages];
-      bool issued[kStages];
-      for (int i = 0; i < kStages; ++i) issued[i] = false;
+      uint32_t n_issued = 0;  // stages issued (the teardown derives each entry's last phase)
       bool ok = true;
       TileCursor cur;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -156,15 +155,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tma_load_5d(s.b[stage], &tmap_b, &s.full[stage], x, 0, 0, n * C::kBlocks, e);
           else
             tma_load_2d(s.b[stage], &tmap_b, &s.full[stage], x, e * p.b_rows + n * BN);
-          issued[stage] = true;
-          issued_phase[stage] = phase;
+          ++n_issued;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
       if (!ok || *(volatile int*)abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
         for (int i = 0; i < kStages; ++i)
-          if (issued[i]) wait_bar_drain(&s.full[i], issued_phase[i]);
+          if (n_issued > (uint32_t)i) wait_bar_drain(&s.full[i], sched::ring_last_phase(n_issued, i, kStages));
       }
     }
   } else if (warp == 1) {

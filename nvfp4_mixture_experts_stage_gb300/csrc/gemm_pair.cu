@@ -144,9 +144,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[kPStages];
-      bool issued[kPStages];
-      for (int i = 0; i < kPStages; ++i) issued[i] = false;
       bool ok = true;
       TileCursor cur;
       // leader addresses of the two copiers' sf_full rings (scalars: a runtime-indexed
@@ -189,8 +186,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           } else {
             tma_load_2d_pair(s.b[stage], &tmap_b, fb, x, e * p.b_rows + n * 256 + 128 * (int)rank);
           }
-          issued[stage] = true;
-          issued_phase[stage] = phase;
           ++g;
           if (++stage == kPStages) { stage = 0; phase ^= 1; }
         }
@@ -200,7 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // leader sees its barriers complete; every load lands within microseconds
         if (rank == 0)
           for (int i = 0; i < kPStages; ++i)
-            if (issued[i]) wait_bar_drain(&s.full[i], issued_phase[i]);
+            if (g > (uint32_t)i) wait_bar_drain(&s.full[i], sched::ring_last_phase(g, i, kPStages));
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 200000ull) {
         }
@@ -209,7 +204,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         // MMA thread that nobody else waits for; it must land in this CTA's empty[i]
         // before the CTA (and its shared memory) is gone.
         for (int i = 0; i < kPStages; ++i)
-          if (issued[i] && !wait_bar_bounded(&s.empty[i], issued_phase[i], abort_flag, p.status)) break;
+          if (g > (uint32_t)i &&
+              !wait_bar_bounded(&s.empty[i], sched::ring_last_phase(g, i, kPStages), abort_flag, p.status))
+            break;
       }
     }
   } else if (warp == 1) {

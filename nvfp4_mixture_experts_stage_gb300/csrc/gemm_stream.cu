@@ -319,9 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[kStages];
-      bool issued[kStages];
-      for (int i = 0; i < kStages; ++i) issued[i] = false;
       bool ok = true;
       // the first n_pre k-blocks: weights now, B rows once the previous kernel is done
       const int n_pre = p.early_weights ? min(kStages, (t_hi - t_lo) * nkb) : 0;
@@ -361,8 +358,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             pre_row[j] = row_x;
           bulk_load(s.sfw[stage], sfw_src + kb * 4 * 512, natoms * 512, &s.full[stage]);
-          issued[stage] = true;
-          issued_phase[stage] = phase;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
           if (++j == n_pre) wait_then_issue_pre_b();
         }
@@ -370,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!waited) wait_then_issue_pre_b();  // no k-blocks, or stopped early
       if (!ok || *(volatile int*)abort_flag)
         for (int i = 0; i < kStages; ++i)
-          if (issued[i]) wait_bar_drain(&s.full[i], issued_phase[i]);
+          if (j > i) wait_bar_drain(&s.full[i], sched::ring_last_phase((uint32_t)j, i, kStages));
     }
   } else if (warp == 1 || warp == 7) {
     // ------------------------------------------------------------ MMA issuers

@@ -34,5 +34,13 @@ MOE_HD bool stream_two_issuers(int nkb) { return nkb % 2 == 0; }
 MOE_HD int stream_first_kb(int r, int nkb) { return stream_two_issuers(nkb) ? r : (r == 0 ? 0 : nkb); }
 MOE_HD int stream_kb_step(int nkb) { return stream_two_issuers(nkb) ? 2 : 1; }
 
+// Producers issue ring stages in order: the k-th stage (k = 0, 1, ...) goes to entry
+// k % stages with phase parity (k / stages) & 1.  After n stages, the parity of entry i's
+// last use (for n > i) -- what a teardown waits for -- is ring_last_phase(n, i, stages),
+// so the producer keeps a count instead of a per-entry record.
+MOE_HD uint32_t ring_last_phase(uint32_t n, int i, int stages) {
+  return ((n - 1u - (uint32_t)i) / (uint32_t)stages) & 1u;
+}
+
 }  // namespace sched
 }  // namespace moe

@@ -17,6 +17,7 @@
 using moe::sched::pair_copier;
 using moe::sched::pair_sf_use;
 using moe::sched::pair_stage;
+using moe::sched::ring_last_phase;
 using moe::sched::stream_first_kb;
 using moe::sched::stream_kb_step;
 
@@ -86,6 +87,27 @@ long stream_always_two(int stages, int nkb, int tiles) {
   return u.violations;
 }
 
+// Producer teardown: after n stages issued in order, the parity of each entry's last use
+// from ring_last_phase against a record kept while issuing (also flags a formula that
+// forgets the wrap: parity = last stage index & 1 instead of its use & 1).
+long ring_teardown(int stages, int n, bool naive) {
+  long bad = 0;
+  long last[16];
+  for (int i = 0; i < stages; ++i) last[i] = -1;
+  int stage = 0;
+  unsigned phase = 0;
+  for (int k = 0; k < n; ++k) {
+    last[stage] = phase;
+    if (++stage == stages) { stage = 0; phase ^= 1u; }
+  }
+  for (int i = 0; i < stages; ++i) {
+    if (n <= i) continue;
+    const unsigned got = naive ? (unsigned)((n - 1 - i) & 1) : ring_last_phase((uint32_t)n, i, stages);
+    if ((long)got != last[i]) ++bad;
+  }
+  return bad;
+}
+
 }  // namespace
 
 int main() {
@@ -107,5 +129,13 @@ int main() {
   std::printf("violations stream %ld\n", scur);
   std::printf("violations stream_always_two_odd %ld\n", sold_odd);
   std::printf("violations stream_always_two_even %ld\n", sold_even);
+  long rcur = 0, rnaive = 0;
+  for (int stages : {4, 5, 6, 8})
+    for (int n = 0; n <= 200; ++n) {
+      rcur += ring_teardown(stages, n, false);
+      rnaive += ring_teardown(stages, n, true);
+    }
+  std::printf("violations ring_teardown %ld\n", rcur);
+  std::printf("violations ring_teardown_naive %ld\n", rnaive);
   return 0;
 }

@@ -35,6 +35,13 @@ def test_current_schedules_never_skip_a_phase(report):
     assert report["stream"] == 0
 
 
+def test_producer_teardown_phase_from_the_stage_count(report):
+    """The producers keep a count of issued stages, not a record per ring entry; the
+    parity of each entry's last use follows from the count."""
+    assert report["ring_teardown"] == 0
+    assert report["ring_teardown_naive"] > 0
+
+
 def test_earlier_schedules_are_flagged(report):
     assert report["pair_shared_barrier"] > 0
     assert report["stream_always_two_odd"] > 0
