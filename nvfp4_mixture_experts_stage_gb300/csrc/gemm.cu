@@ -186,9 +186,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sf = tmem + C::kSfBase + stage * C::kSfCols;
           const uint64_t da = da0 + (uint64_t)((stage * C::kAStage) >> 4);
           const uint64_t db = db0 + (uint64_t)((stage * C::kBStage) >> 4);
-          for (int kk = 0; kk < natoms; ++kk)
-            tc_mma_fp4(tmem, da + 2 * kk, db + 2 * kk, C::kIdesc, sf + 4 * kk, sf + 16 + C::kSfbPerStep * kk,
-                       (kb | kk) != 0);
+          if (natoms == 4) {  // every k-block but a short last one: no loop overhead between MMAs
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_fp4(tmem, da + 2 * kk, db + 2 * kk, C::kIdesc, sf + 4 * kk, sf + 16 + C::kSfbPerStep * kk,
+                         (kb | kk) != 0);
+          } else {
+            for (int kk = 0; kk < natoms; ++kk)
+              tc_mma_fp4(tmem, da + 2 * kk, db + 2 * kk, C::kIdesc, sf + 4 * kk, sf + 16 + C::kSfbPerStep * kk,
+                         (kb | kk) != 0);
+          }
           tc_commit(&s.empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }

@@ -227,8 +227,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint32_t sf = tmem + kPSfBase + stage * kPSfCols;
           const uint64_t da = da0 + (uint64_t)((stage * kPAStage) >> 4);
           const uint64_t db = db0 + (uint64_t)((stage * kPBStage) >> 4);
-          for (int kk = 0; kk < natoms; ++kk)
-            tc_mma_fp4_pair(tmem, da + 2 * kk, db + 2 * kk, kPIdesc, sf + 4 * kk, sf + 16 + 8 * kk, (kb | kk) != 0);
+          if (natoms == 4) {  // every k-block but a short last one: no loop overhead between MMAs
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_fp4_pair(tmem, da + 2 * kk, db + 2 * kk, kPIdesc, sf + 4 * kk, sf + 16 + 8 * kk,
+                              (kb | kk) != 0);
+          } else {
+            for (int kk = 0; kk < natoms; ++kk)
+              tc_mma_fp4_pair(tmem, da + 2 * kk, db + 2 * kk, kPIdesc, sf + 4 * kk, sf + 16 + 8 * kk,
+                              (kb | kk) != 0);
+          }
           tc_commit_pair_mc(&s.empty[stage], 0x3);
           if (++stage == kPStages) { stage = 0; phase ^= 1; }
         }
@@ -250,8 +258,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (rank == 0 && lane == 0) {
       const uint64_t dsa0 = sdesc_sf(s.sfa[0]), dsb0 = sdesc_sf(s.sfb[0]);
       const int c = warp - 2;
+      int kb = c % nkb;  // g % nkb, advanced by 2 per stage
       for (int g = c; g < my_stages; g += 2) {  // the stages with sched::pair_copier(g) == c
-        const int kb = g % nkb;
         const int natoms = min(4, ksf4 - 4 * kb);
         const int stage = (int)sched::pair_stage((uint32_t)g, kPStages);
         const uint32_t phase = sched::pair_sf_use((uint32_t)g, kPStages) & 1;
@@ -260,12 +268,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const uint32_t sf = tmem + kPSfBase + stage * kPSfCols;
         const uint64_t dsa = dsa0 + (uint64_t)((stage * kPSfaStage) >> 4);
         const uint64_t dsb = dsb0 + (uint64_t)((stage * kPSfbStage) >> 4);
-        for (int kk = 0; kk < natoms; ++kk) {
-          tc_cp_sf_pair(sf + 4 * kk, dsa + 32 * kk);
-          tc_cp_sf_pair(sf + 16 + 8 * kk, dsb + 32 * kk);
-          tc_cp_sf_pair(sf + 16 + 8 * kk + 4, dsb + 128 + 32 * kk);
+        if (natoms == 4) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc_cp_sf_pair(sf + 4 * kk, dsa + 32 * kk);
+            tc_cp_sf_pair(sf + 16 + 8 * kk, dsb + 32 * kk);
+            tc_cp_sf_pair(sf + 16 + 8 * kk + 4, dsb + 128 + 32 * kk);
+          }
+        } else {
+          for (int kk = 0; kk < natoms; ++kk) {
+            tc_cp_sf_pair(sf + 4 * kk, dsa + 32 * kk);
+            tc_cp_sf_pair(sf + 16 + 8 * kk, dsb + 32 * kk);
+            tc_cp_sf_pair(sf + 16 + 8 * kk + 4, dsb + 128 + 32 * kk);
+          }
         }
         tc_commit_pair_mc(&s.full[stage], 0x1);  // the leader's barrier, once the copies are done
+        kb += 2;
+        while (kb >= nkb) kb -= nkb;  // nkb may be 1
       }
     }
   } else {
