@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       int it = 0;
       const uint64_t da0 = sdesc_sw128(s.a[0]), db0 = sdesc_sw128(s.b[0]);
+      // this stage's scale columns and operand descriptors, advanced with the ring position
+      // (register updates after each commit, not a multiply before each stage's first MMA)
+      uint32_t sf = tmem + C::kSfBase;
+      uint64_t da = da0, db = db0;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++it) {
         if (!wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -183,9 +187,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sf = tmem + C::kSfBase + stage * C::kSfCols;
-          const uint64_t da = da0 + (uint64_t)((stage * C::kAStage) >> 4);
-          const uint64_t db = db0 + (uint64_t)((stage * C::kBStage) >> 4);
           if (natoms == 4) {  // every k-block but a short last one: no loop overhead between MMAs
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -197,7 +198,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                          (kb | kk) != 0);
           }
           tc_commit(&s.empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+            sf = tmem + C::kSfBase;
+            da = da0;
+            db = db0;
+          } else {
+            sf += C::kSfCols;
+            da += (uint64_t)(C::kAStage >> 4);
+            db += (uint64_t)(C::kBStage >> 4);
+          }
         }
         if (!ok) break;
         tc_commit(&s.tfull);
@@ -224,14 +235,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sf = tmem + C::kSfBase + stage * C::kSfCols;
           const uint64_t dsa = dsa0 + (uint64_t)((stage * C::kSfaStage) >> 4);
           const uint64_t dsb = dsb0 + (uint64_t)((stage * C::kSfbStage) >> 4);
+          if (natoms == 4) {  // every k-block but a short last one: the copies back to back
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int kk = 2 * c + h;
-            if (kk < natoms) {
+            for (int h = 0; h < 2; ++h) {
+              const int kk = 2 * c + h;
               tc_cp_sf(sf + 4 * kk, dsa + 32 * kk);
 #pragma unroll
               for (int j = 0; j < C::kBlocks; ++j)
                 tc_cp_sf(sf + 16 + C::kSfbPerStep * kk + 4 * j, dsb + 128 * j + 32 * kk);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int kk = 2 * c + h;
+              if (kk < natoms) {
+                tc_cp_sf(sf + 4 * kk, dsa + 32 * kk);
+#pragma unroll
+                for (int j = 0; j < C::kBlocks; ++j)
+                  tc_cp_sf(sf + 16 + C::kSfbPerStep * kk + 4 * j, dsb + 128 * j + 32 * kk);
+              }
             }
           }
           tc_commit(&s.full[stage]);  // arrives once this warp's copies are done

@@ -217,6 +217,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       int it = 0;
       const uint64_t da0 = sdesc_sw128(s.a[0]), db0 = sdesc_sw128(s.b[0]);
+      // this stage's scale columns and operand descriptors, advanced with the ring position
+      uint32_t sf = tmem + kPSfBase;
+      uint64_t da = da0, db = db0;
       for (int t = pair; t < total_tiles && ok; t += npairs, ++it) {
         if (!wait_bar_bounded(&s.tempty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -224,9 +227,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const int natoms = min(4, ksf4 - 4 * kb);
           if (!wait_bar_bounded(&s.full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sf = tmem + kPSfBase + stage * kPSfCols;
-          const uint64_t da = da0 + (uint64_t)((stage * kPAStage) >> 4);
-          const uint64_t db = db0 + (uint64_t)((stage * kPBStage) >> 4);
           if (natoms == 4) {  // every k-block but a short last one: no loop overhead between MMAs
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -238,7 +238,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                               (kb | kk) != 0);
           }
           tc_commit_pair_mc(&s.empty[stage], 0x3);
-          if (++stage == kPStages) { stage = 0; phase ^= 1; }
+          if (++stage == kPStages) {
+            stage = 0;
+            phase ^= 1;
+            sf = tmem + kPSfBase;
+            da = da0;
+            db = db0;
+          } else {
+            sf += kPSfCols;
+            da += (uint64_t)(kPAStage >> 4);
+            db += (uint64_t)(kPBStage >> 4);
+          }
         }
         if (!ok) break;
         tc_commit_pair_mc(&s.tfull, 0x3);
