@@ -137,10 +137,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // prepared weight row blocks n*kBlocks .. n*kBlocks + kBlocks - 1 of expert e
         const int sfb_block = e * (p.b_rows >> 7) + n * C::kBlocks;
         // four loads per stage (the producer's issue time, not the bytes, bounds how fast
-        // stages arrive): the A scale atoms; the weight scale atoms of all kBlocks blocks in
-        // one 3-D box (a short last stage reads zeros past the row end); A rows; the tile's
+        // stages arrive): the weight scale atoms of all kBlocks blocks in one 3-D box (a short
+        // last stage reads zeros past the row end); the A scale atoms; A rows; the tile's
         // weight rows in one box (L1: kBlocks blocks of 64 gate then 64 up rows, a 5-D box).
-        // The scales go first: their copies into tensor memory are on the path from a
+        // The scales go first (the weight scales' 3-D box before the activation scales' bulk
+        // copy, which lands sooner): their copies into tensor memory are on the path from a
         // stage's release to its MMAs, and they then land ahead of the operand bytes.
         for (int kb = 0; kb < nkb; ++kb) {
           const int natoms = min(4, ksf4 - 4 * kb);
@@ -148,8 +149,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&s.sf_full[stage], natoms * 512 + C::kSfbStage);
           mbar_arrive_expect_tx(&s.full[stage], C::kAStage + C::kBStage);
           const int x = kb * kBKBytes;
-          bulk_load(s.sfa[stage], sfa_src + kb * 4 * 512, natoms * 512, &s.sf_full[stage]);
           tma_load_3d(s.sfb[stage], &tmap_sfb, &s.sf_full[stage], 0, 8 * kb, sfb_block);
+          bulk_load(s.sfa[stage], sfa_src + kb * 4 * 512, natoms * 512, &s.sf_full[stage]);
           tma_load_2d(s.a[stage], &tmap_a, &s.full[stage], x, row_a);
           if (kL1)
             tma_load_5d(s.b[stage], &tmap_b, &s.full[stage], x, 0, 0, n * C::kBlocks, e);

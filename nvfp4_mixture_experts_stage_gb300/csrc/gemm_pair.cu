@@ -177,8 +177,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint32_t sfb = (sched::pair_copier(g) ? sf_full_c1 : sf_full_c0) + 8 * stage,
                          fb = full0 + 8 * stage;
           const int x = kb * kBKBytes;
-          if (has_rows) tma_load_2d_pair(s.sfa[stage], &tmap_sfa, sfb, 0, sfa_row + 8 * kb);
           tma_load_3d_pair(s.sfb[stage], &tmap_sfb, sfb, 0, 8 * kb, sfb_block);
+          if (has_rows) tma_load_2d_pair(s.sfa[stage], &tmap_sfa, sfb, 0, sfa_row + 8 * kb);
           if (has_rows) tma_load_2d_pair(s.a[stage], &tmap_a, fb, x, row_a);
           if (kL1) {
             // prepared block 2n + rank: 64 gate rows then the matching 64 up rows (one 5-D box)
