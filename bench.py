@@ -45,20 +45,20 @@ METRIC = "MoE layer tokens/s; grouped-GEMM NVFP4 TFLOPS as % of GB300 dense FP4 
 # files that kernel is compiled from hash to the captured ones.
 NCU_TRAFFIC = {
     ("decode", "auto", "gemm_l1"): {
-        "bytes": 670396416 + 3520512,
+        "bytes": 670416896 + 3473920,
         "kernel_sources": ("gemm_stream.cu", "pipeline.cuh", "tcgen05.cuh", "common.cuh"),
         "sources_sha256_16": "ea0dcb4acfdf0840",
     },
     ("prefill", "auto", "gemm_l1"): {
-        "bytes": 837367296 + 106026496,
+        "bytes": 837377536 + 106087936,
         "kernel_sources": ("gemm.cu", "gemm_tiled.cuh", "tcgen05.cuh", "kernels.cuh", "common.cuh"),
-        "sources_sha256_16": "d6d1a199dcea5b21",
+        "sources_sha256_16": "01acab902e6aa385",
     },
     ("prefill", "auto", "gemm_l2"): {
-        "bytes": 458223104 + 485961216,
+        "bytes": 458414848 + 486668544,
         "kernel_sources": ("gemm_pair.cu", "gemm_tiled.cuh", "pipeline.cuh", "tcgen05.cuh", "kernels.cuh",
                            "common.cuh"),
-        "sources_sha256_16": "cff17518eca2f6a1",
+        "sources_sha256_16": "844347ff2bf33b45",
     },
 }
 
