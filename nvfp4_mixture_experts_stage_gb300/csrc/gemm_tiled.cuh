@@ -115,9 +115,8 @@ MOE_DEV void epilogue_load(uint32_t taddr, int half, float (&v)[BN / 2]) {
     // BN 128: half h = gate columns 32h.., up columns 64 + 32h..
     constexpr int G = kCols / 2;
     const uint32_t g0 = BN == 256 ? 128 * half : 32 * half;
-    if constexpr (G == 64) {
-      tmem_ld64(taddr + g0, *reinterpret_cast<float(*)[64]>(&v[0]));
-      tmem_ld64(taddr + g0 + 64, *reinterpret_cast<float(*)[64]>(&v[G]));
+    if constexpr (G == 64) {  // gate columns g0.. then up columns g0 + 64..: one 128-column load
+      tmem_ld128(taddr + g0, *reinterpret_cast<float(*)[128]>(&v[0]));
     } else {
 #pragma unroll
       for (int j = 0; j < G; j += 16) {
@@ -126,7 +125,9 @@ MOE_DEV void epilogue_load(uint32_t taddr, int half, float (&v)[BN / 2]) {
       }
     }
   } else {
-    if constexpr (kCols % 64 == 0) {
+    if constexpr (kCols == 128) {
+      tmem_ld128(taddr + half * kCols, *reinterpret_cast<float(*)[128]>(&v[0]));
+    } else if constexpr (kCols % 64 == 0) {
 #pragma unroll
       for (int j = 0; j < kCols; j += 64)
         tmem_ld64(taddr + half * kCols + j, *reinterpret_cast<float(*)[64]>(&v[j]));
