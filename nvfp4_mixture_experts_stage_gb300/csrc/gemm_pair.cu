@@ -17,9 +17,9 @@
 //
 // Cluster of two CTAs, 12 warps each, one CTA per SM.  Rank 0 leads; every barrier
 // the pipeline runs on lives in the leader except each CTA's empty[s] and tfull.
-//   warp 0 (both)      TMA producer: this CTA's scale atoms first (the A atoms of its rows,
-//                      the B atoms of all 256 weight rows: the MMA reads every B scale
-//                      from the local TMEM), then its A rows and its 128 weight rows, into
+//   warp 0 (both)      TMA producer: this CTA's scale atoms first (the B atoms of all 256
+//                      weight rows, since the MMA reads every B scale from the local TMEM,
+//                      then the A atoms of its rows), then its A rows and its 128 weight rows, into
 //                      a five-stage ring.  The loads use the CTA-pair form of TMA, so the
 //                      peer's bytes count directly on the leader's sf_full[c][s] (scales) and
 //                      full[s] (operands); the leader's producer arms both with the bytes
