@@ -55,10 +55,10 @@ NCU_TRAFFIC = {
         "sources_sha256_16": "c3268b0e9f82639b",
     },
     ("prefill", "auto", "gemm_l2"): {
-        "bytes": 458345984 + 486477568,
+        "bytes": 458267392 + 486686720,
         "kernel_sources": ("gemm_pair.cu", "gemm_tiled.cuh", "pipeline.cuh", "tcgen05.cuh", "kernels.cuh",
                            "common.cuh"),
-        "sources_sha256_16": "2847520b42d0a948",
+        "sources_sha256_16": "23b28a7704de572e",
     },
 }
 
